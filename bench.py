@@ -1,0 +1,478 @@
+"""Decode benchmark: paged split-KV decode attention on GB300.
+
+One step = one pd_decode (split-KV partial kernel + combine kernel) over the
+whole batch of the Llama-3-8B-shaped workload (32 sequences, 32 q / 8 kv
+heads, head_dim 128, block_size 16, lengths uniform in [1024, 4096], BF16
+cache, pages shuffled across the pool, splits chosen automatically), inputs
+resident in HBM. Reported value: KV-read GB/s = algorithmic bytes / step time
+(us/step alongside); e2e: the same through the C ABI from pinned host inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pd|reference]
+                    [--workload llama8b|long_b4_32k|...] [--splits S]
+
+With torchrun (N > 1) every rank decodes its own independent batch (seeded by
+rank, replicas only: no data is exchanged); the barrier and max-over-ranks
+timing use torch.distributed.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode µs/step and KV-read HBM GB/s (% of GB300 peak) at 1 GPU"
+ELEM_BYTES = {0: 2.0, 1: 1.0, 2: 0.5625}
+DTYPE_NAME = {0: "bf16", 1: "fp8_e4m3", 2: "nvfp4"}
+PARTIAL_KERNEL_SRC = ["paged_kv_split_gb300/csrc/decode_simple.cu",
+                      "paged_kv_split_gb300/csrc/pd_common.cuh"]
+
+
+def workload(name: str, rank: int = 0):
+    from paged_kv_split_gb300 import inputs as I
+    seed = 1000 * rank
+    table = {
+        "llama8b": lambda: I.llama8b(seed=seed),
+        "long_b1_32k": lambda: I.long_context(1, 32768, seed=seed),
+        "long_b4_32k": lambda: I.long_context(4, 32768, seed=seed),
+        "long_b4_8k": lambda: I.long_context(4, 8192, seed=seed),
+        "wide_d512": lambda: I.wide_head(seed=seed),
+        "window_d256": lambda: I.sliding(seed=seed),
+        "quant_fp8": lambda: I.quantised(1, seed=seed),
+        "quant_nvfp4": lambda: I.quantised(2, seed=seed),
+    }
+    return table[name]()
+
+
+def algorithmic_bytes(case, kv_dtype) -> dict:
+    """KV bytes read over the window + q + out + block-table entries touched."""
+    L = case.seq_lens.astype(np.int64)
+    W = case.sliding_window
+    lo = np.where((W > 0) & (L > W), L - W, 0)
+    keys = int((L - lo).sum())
+    bs = case.block_size
+    pages = int(np.where(L > lo, (L - 1) // bs - lo // bs + 1, 0).sum())
+    kv = keys * case.num_kv_heads * 2 * case.head_dim * ELEM_BYTES[kv_dtype]
+    q = case.num_seqs * case.num_q_heads * case.head_dim * 2
+    return {"kv": kv, "q": q, "out": q, "table": 4 * pages, "total": kv + 2 * q + 4 * pages,
+            "keys": keys}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in PARTIAL_KERNEL_SRC:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name: str):
+    """Per-launch DRAM bytes of the partial kernel from a committed ncu
+    summary, if it was captured from the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload_name)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms in the background."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid: str | None):
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "50"]
+            if gpu_uuid:
+                cmd += ["-i", gpu_uuid]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        win = [s for t, s in self.samples if t0 <= t <= t1]
+        if not win:  # a very short timed region: take the nearest samples after it
+            win = [s for t, s in self.samples if t > t1][:2]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in win if num(s[0]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in win:
+            for k, name in enumerate(names):
+                if len(s) > 4 + k and s[4 + k].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(win[0][1]) if len(win[0]) > 1 else None,
+                "reasons": sorted(reasons), "samples": len(win)}
+
+
+def dist_init(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+def time_oracle(case, kv_dtype, kc_host, vc_host, ks, vs, budget_s: float):
+    """The oracle as it stands, single-threaded, on a bounded sample (the first
+    k sequences of the batch, k grown until one call takes ~budget_s)."""
+    import oracle
+    orc = oracle.get()
+    k = 1
+    while True:
+        t = time.perf_counter()
+        orc.decode(case.q[:k], kc_host, vc_host, case.block_tables[:k], case.seq_lens[:k],
+                   case.num_kv_heads, case.block_size, case.num_blocks, case.scale,
+                   case.sliding_window, kv_dtype, ks, vs)
+        dt = time.perf_counter() - t
+        if dt >= budget_s or k >= case.num_seqs:
+            break
+        k = min(case.num_seqs, max(k + 1, int(k * budget_s / max(dt, 1e-3))))
+    sub = type(case)(**{**case.__dict__})
+    sub.seq_lens = case.seq_lens[:k]
+    sub.num_seqs = k
+    sub.q = case.q[:k]
+    ab = algorithmic_bytes(sub, kv_dtype)
+    return k, dt, ab
+
+
+def build_device_state(case, kv_dtype, replicas, dev):
+    import torch
+    from paged_kv_split_gb300 import binding as pd
+
+    def bf16(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    key, value = bf16(case.key), bf16(case.value)
+    slots = torch.from_numpy(case.slot_mapping).to(dev)
+    ks = vs = 1.0
+    if kv_dtype == 1:
+        ks, vs = pd.fp8_calibrate(key, value)
+    caches = []
+    for _ in range(replicas):
+        kc = pd.empty_cache(kv_dtype, case.num_blocks, case.block_size, case.num_kv_heads,
+                            case.head_dim, dev)
+        vc = torch.empty_like(kc)
+        kc.zero_()
+        vc.zero_()
+        pd.pd_reshape_and_cache(key, value, kc, vc, slots, num_blocks=case.num_blocks,
+                                block_size=case.block_size, kv_dtype=kv_dtype, k_scale=ks,
+                                v_scale=vs)
+        caches.append((kc, vc))
+    del key, value
+    return caches, ks, vs
+
+
+def run_pd(args, rank, world, local):
+    import torch
+    from paged_kv_split_gb300 import binding as pd
+
+    dev = torch.device("cuda", local if world > 1 else 0)
+    case = workload(args.workload, rank)
+    kv_dtype = case.kv_dtype
+    ab = algorithmic_bytes(case, kv_dtype)
+    cache_bytes = pd.pd_cache_bytes(kv_dtype, case.num_blocks, case.block_size,
+                                    case.num_kv_heads, case.head_dim)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    replicas = max(2, math.ceil(3 * l2 / max(2 * cache_bytes, 1)))
+    caches, ks, vs = build_device_state(case, kv_dtype, replicas, dev)
+    q = torch.from_numpy(case.q.view(np.int16)).to(dev).view(torch.bfloat16)
+    bt = torch.from_numpy(case.block_tables).to(dev)
+    lens = torch.from_numpy(case.seq_lens).to(dev)
+    out = torch.empty_like(q)
+    B, hq, D = case.q.shape
+    mbs = case.max_blocks_per_seq
+    S = args.splits or pd.pd_choose_num_splits(B, case.num_kv_heads, mbs, case.block_size,
+                                               case.sliding_window, D, kv_dtype, dev.index)
+    ws = torch.empty(pd.pd_decode_workspace_bytes(B, hq, D, S), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    common = dict(num_kv_heads=case.num_kv_heads, block_size=case.block_size,
+                  num_blocks=case.num_blocks, scale=case.scale, num_splits=S,
+                  sliding_window=case.sliding_window, kv_dtype=kv_dtype, k_scale=ks, v_scale=vs)
+
+    def step(i, ev=None):
+        kc, vc = caches[i % replicas]
+        if ev is not None:
+            ev[0].record(stream)
+        pd.pd_decode_partial(q, kc, vc, bt, lens, ws, **common)
+        if ev is not None:
+            ev[1].record(stream)
+        pd.pd_decode_combine(ws, lens, out, block_size=case.block_size, max_blocks_per_seq=mbs,
+                             num_splits=S, sliding_window=case.sliding_window)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    w0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(i, evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    w1 = time.time()
+    barrier(world)
+    total_ms = start.elapsed_time(end)
+    partial_ms = [a.elapsed_time(b) for a, b in evs]
+    time.sleep(0.1)
+    sampler.stop()
+    clocks = sampler.summary(w0, w1)
+
+    ms_step_local = total_ms / args.steps
+    ms_step = max_over_ranks(ms_step_local, world)
+    total_bytes = sum_over_ranks(ab["total"], world)
+    value = total_bytes / (ms_step * 1e-3) / 1e9
+
+    # roofline of the dominant kernel (the split-KV partial)
+    part_ms = statistics.mean(partial_ms)
+    partial_bytes = ab["kv"] + ab["q"] + ab["table"]
+    peak, peak_kind = measured_peaks()
+    achieved = partial_bytes / (part_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "split-KV partial", "achieved": round(achieved, 1),
+                "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(args.workload),
+                "algorithmic_bytes_per_launch": int(partial_bytes),
+                "partial_us_per_launch": round(part_ms * 1e3, 2)}
+
+    # e2e: through the C ABI from pinned host buffers, copies inside the timing
+    q_h = torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    bt_h = torch.from_numpy(case.block_tables).pin_memory()
+    lens_h = torch.from_numpy(case.seq_lens).pin_memory()
+    out_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    q_d, bt_d, lens_d = torch.empty_like(q), torch.empty_like(bt), torch.empty_like(lens)
+    e2e_steps = max(10, min(args.steps, 200))
+
+    def e2e_step(i):
+        kc, vc = caches[i % replicas]
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        lens_d.copy_(lens_h, non_blocking=True)
+        pd.pd_decode(q_d, kc, vc, bt_d, lens_d, out, workspace=ws, **common)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(3):
+        e2e_step(i)
+    barrier(world)
+    t = time.perf_counter()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e2e_s = max_over_ranks((time.perf_counter() - t) / e2e_steps, world)
+    h2d = q_h.numel() * 2 + bt_h.numel() * 4 + lens_h.numel() * 4
+    d2h = out_h.numel() * 2
+    e2e = {"value": round(total_bytes / e2e_s / 1e9, 1), "unit": "GB/s",
+           "us_per_step": round(e2e_s * 1e6, 2), "h2d_bytes_per_step": int(h2d),
+           "d2h_bytes_per_step": int(d2h)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        kc, vc = caches[0]
+        k, dt, sab = time_oracle(case, kv_dtype, kc.cpu().numpy(), vc.cpu().numpy(), ks, vs,
+                                 args.cpu_budget)
+        cpu = {"value": round(sab["total"] / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "us_per_step_sample": round(dt * 1e6, 1),
+               "sample": f"first {k} of {case.num_seqs} sequences of the same batch "
+                         f"({sab['keys']} keys), one single-threaded oracle_decode call"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+            "us_per_step": round(ms_step * 1e3, 2),
+            "pct_of_hbm_peak": round(100 * value / peak, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": DTYPE_NAME[kv_dtype], "data": "synthetic",
+            "config": {"workload": args.workload, "num_seqs": B, "num_q_heads": hq,
+                       "num_kv_heads": case.num_kv_heads, "head_dim": D,
+                       "block_size": case.block_size, "kv_dtype": DTYPE_NAME[kv_dtype],
+                       "sliding_window": case.sliding_window, "num_splits": S,
+                       "keys_per_step": ab["keys"], "algorithmic_bytes_per_step": int(ab["total"]),
+                       "workspace_bytes_per_step": int(2 * B * hq * S * (D + 2) * 4),
+                       "l2": f"inputs larger than L2: {replicas} cache replicas of "
+                             f"{2 * cache_bytes / 1e6:.0f} MB rotated per step "
+                             f"(L2 {l2 / 1e6:.0f} MB)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 2 * args.steps, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, timed on host cores, on a bounded sample."""
+    if rank != 0:
+        return
+    case = workload(args.workload, 0)
+    kv_dtype = case.kv_dtype
+    import oracle
+    orc = oracle.get()
+    ks = vs = 1.0
+    if kv_dtype == 1:
+        ks = orc.fp8_scale(orc.absmax_bf16(case.key))
+        vs = orc.fp8_scale(orc.absmax_bf16(case.value))
+    n = orc.cache_bytes(kv_dtype, case.num_blocks, case.block_size, case.num_kv_heads,
+                        case.head_dim)
+    kc = np.zeros(n, np.uint8)
+    vc = np.zeros(n, np.uint8)
+    orc.reshape_and_cache(case.key, case.value, kc, vc, case.slot_mapping, case.num_kv_heads,
+                          case.head_dim, case.block_size, case.num_blocks, kv_dtype, ks, vs)
+    per_step = min(2.0, 150.0 / max(args.steps + args.warmup, 1))
+    k, _, sab = time_oracle(case, kv_dtype, kc, vc, ks, vs, per_step)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t = time.perf_counter()
+        orc.decode(case.q[:k], kc, vc, case.block_tables[:k], case.seq_lens[:k],
+                   case.num_kv_heads, case.block_size, case.num_blocks, case.scale,
+                   case.sliding_window, kv_dtype, ks, vs)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t)
+    s = sum(times) / len(times)
+    value = sab["total"] / s / 1e9
+    sample = (f"first {k} of {case.num_seqs} sequences ({sab['keys']} keys) per step, "
+              f"single-threaded oracle_decode")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": DTYPE_NAME[kv_dtype], "data": "synthetic",
+        "config": {"workload": args.workload, "num_seqs": case.num_seqs,
+                   "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads,
+                   "head_dim": case.head_dim, "block_size": case.block_size,
+                   "kv_dtype": DTYPE_NAME[kv_dtype]},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="pd", choices=["pd", "reference"])
+    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=3.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    from paged_kv_split_gb300 import build as pd_build
+    pd_build.build()
+    rank, world, local = dist_init(args)
+    try:
+        run_pd(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

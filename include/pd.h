@@ -1,0 +1,205 @@
+/*
+ * pd.h - C ABI of libpd.so: paged split-KV decode attention on GB300 (sm_103a).
+ *
+ * Every operation here is one step of single-token (decode) attention for a
+ * batch of sequences whose keys and values live in a paged KV cache read
+ * through a block table, with grouped-query heads, cut into split-KV
+ * partials that a log-sum-exp combine merges. The passages each call follows
+ * are cited beside it:
+ *   [metrale]   docs.metrale.ai, "prefill_attn_b.rs" (launchers for the NVFP4
+ *               cache write, `bf16_absmax`, `paged_decode_attn_splitk_*` and
+ *               `paged_decode_attn_reduce_*`);
+ *   [AstrAI]    "ViperEkura/AstrAI csrc/tests" commit log (split-KV decode
+ *               with o_part / ml_part and a single combine kernel,
+ *               compute_num_splits, int32 indices, divisibility checks);
+ *   [pegainfer] pegainfer issue 1008 (paged decode / split-KV decode units).
+ *
+ * Conventions for every call:
+ *   - Pointers named as device memory must be device pointers (or managed
+ *     memory) owned by the caller; the library keeps no reference after the
+ *     call returns, allocates nothing and never synchronises.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). All work is enqueued on it, in order.
+ *   - Every device pointer must be 16-byte aligned.
+ *   - Return value: PD_OK, or a pd_status code; nothing throws. Argument
+ *     errors are reported before anything is enqueued. PD_ERR_CUDA means a
+ *     launch failed (cudaGetLastError was not cudaSuccess).
+ *   - bf16 tensors are IEEE bfloat16 bit patterns (uint16).
+ *
+ * Cache layouts (per K cache and per V cache; kv_dtype selects the form):
+ *   PD_KV_BF16      page = bf16 [block_size][num_kv_heads][head_dim]
+ *                   ([metrale] "the cache is [blocks, block_size, kv_heads,
+ *                   head_dim] and the kernel computes the page stride").
+ *   PD_KV_FP8_E4M3  page = E4M3 bytes [block_size][num_kv_heads][head_dim];
+ *                   value = decode(byte) * k_scale (or v_scale), per-tensor
+ *                   fp32 scales ([metrale] `paged_decode_attn_splitk_fp8`,
+ *                   k_scale / v_scale / cache_stride).
+ *   PD_KV_NVFP4     page = data section E2M1 nibbles
+ *                   [num_kv_heads][block_size][head_dim/2] (element 2i in the
+ *                   low nibble) followed by the scale section, one E4M3 byte
+ *                   per 16 elements [num_kv_heads][block_size][head_dim/16];
+ *                   the page stride is rounded up to a multiple of 128 bytes
+ *                   ([metrale] `reshape_and_cache_nvfp4`: "E2M1 values with
+ *                   one E4M3 scale per 16", block_stride_bytes,
+ *                   data_section_bytes). The order inside each section is
+ *                   this library's choice; the pages leave it open.
+ *   Slot s of the pool is page s / block_size, row s % block_size.
+ */
+#ifndef PD_H_
+#define PD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+enum pd_status {
+  PD_OK = 0,
+  PD_ERR_INVALID_ARG = 1,         /* null / misaligned pointer, bad size or shape */
+  PD_ERR_UNSUPPORTED = 2,         /* head_dim, block_size, group size or dtype not built */
+  PD_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < pd_decode_workspace_bytes(...) */
+  PD_ERR_CUDA = 4                 /* a CUDA runtime call or kernel launch failed */
+};
+
+/* KV cache forms. */
+enum pd_kv_dtype { PD_KV_BF16 = 0, PD_KV_FP8_E4M3 = 1, PD_KV_NVFP4 = 2 };
+
+/* Device-side status bits, accumulated by the kernels (see pd_device_status). */
+enum pd_device_flag {
+  PD_DEV_BAD_PAGE = 1,    /* a block_tables entry was < 0 or >= num_blocks: page skipped */
+  PD_DEV_BAD_SEQ_LEN = 2, /* seq_lens[b] < 0 or > max_blocks_per_seq*block_size: clamped */
+  PD_DEV_BAD_SLOT = 4     /* slot_mapping[t] >= num_blocks*block_size: token skipped */
+};
+
+/* Human-readable name of a pd_status value (static string, never NULL). */
+const char* pd_status_string(int status);
+
+/* Bytes of one K (or one V) cache of num_blocks pages in the given form.
+ * Returns 0 for an unsupported combination. Host-only, no CUDA call. */
+size_t pd_cache_bytes(int32_t kv_dtype, int64_t num_blocks, int32_t block_size,
+                      int32_t num_kv_heads, int32_t head_dim);
+
+/* Bytes of one page (the page stride) in the given form; 0 if unsupported. */
+size_t pd_page_bytes(int32_t kv_dtype, int32_t block_size, int32_t num_kv_heads,
+                     int32_t head_dim);
+
+/* Write (and quantise) each token's K and V rows into the paged caches at
+ * slot_mapping[t] ([metrale] `reshape_and_cache_nvfp4`: "Write each token's
+ * K and V into the paged NVFP4 cache at its slot_mapping slot", extended to
+ * the BF16 and FP8 forms that the decode launchers read).
+ *   key, value    device bf16 [num_tokens][num_kv_heads][head_dim], contiguous.
+ *   k_cache,      device caches of pd_cache_bytes(kv_dtype, num_blocks, ...)
+ *   v_cache       bytes each; only the slots named by slot_mapping change.
+ *   slot_mapping  device int32 [num_tokens]; a negative slot skips the token
+ *                 (padding); a slot >= num_blocks*block_size is skipped and
+ *                 flagged PD_DEV_BAD_SLOT.
+ *   BF16 copies the bit patterns. FP8 stores E4M3(float(x) / scale) with
+ *   IEEE fp32 division, round to nearest even and saturation to +-448
+ *   (NaN -> 0x7F|sign). NVFP4 stores, per 16 consecutive elements of a
+ *   (token, head) row, scale = E4M3(amax / 6) with amax = max |x| (NaN
+ *   skipped) and codes E2M1(float(x) / decode(scale)) rounded to nearest
+ *   even and saturated to +-6 (NaN -> +-6); a group whose scale decodes to 0
+ *   stores +0 codes. k_scale / v_scale are read only for FP8 and must then be
+ *   finite and > 0.
+ * head_dim in {64, 128, 256, 512}; block_size in {16, 32}; num_tokens >= 0. */
+int pd_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                         const int32_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                         int32_t kv_dtype, float k_scale, float v_scale, void* stream);
+
+/* Max |x| over n bf16 values, folded into *out_max with an atomic max
+ * ([metrale] `bf16_absmax`: "The caller zeroes out_max first"). NaN values
+ * are skipped. data: device bf16 [n]; out_max: device float, caller-zeroed.
+ * Used for FP8 calibration: k_scale = absmax(K) / 448 (1 if absmax is 0). */
+int pd_absmax_bf16(const void* data, int64_t n, float* out_max, void* stream);
+
+/* Workspace bytes that pd_decode / pd_decode_partial need for num_splits
+ * partials: per (sequence, q head, split) head_dim fp32 values of the
+ * normalised partial output plus its running max m and sum l ([metrale]:
+ * "The workspace is F32 [head_dim values, m, l] per split"). */
+size_t pd_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                 int32_t num_splits);
+
+/* Split count chosen from the SM count of `device` and the number of page
+ * tiles ([AstrAI] compute_num_splits "only use base_blocks and
+ * tiles_total"; short sequences get more splits). Returns S >= 1, or a
+ * negative pd_status on error. Depends only on the shapes, never on the
+ * contents of seq_lens, so it needs no device read. */
+int pd_choose_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_blocks_per_seq,
+                         int32_t block_size, int32_t sliding_window, int32_t head_dim,
+                         int32_t kv_dtype, int device);
+
+/* The same choice with the SM count given (no CUDA call). */
+int pd_plan_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_blocks_per_seq,
+                       int32_t block_size, int32_t sliding_window, int32_t num_sms);
+
+/* One decode step: split-KV partials then the log-sum-exp combine.
+ * out[b, h, :] = bf16( sum_j e_j v_j / sum_j e_j ), e_j = exp(s_j - max s),
+ * s_j = scale * (q[b, h, :] . k_j), over the keys j of sequence b inside the
+ * window, k_j / v_j read from page block_tables[b, j / block_size], row
+ * j % block_size, kv head h / (num_q_heads / num_kv_heads).
+ *   q             device bf16 [num_seqs][num_q_heads][head_dim], contiguous.
+ *   k_cache,      device caches in the kv_dtype form (layout above).
+ *   v_cache
+ *   block_tables  device int32 [num_seqs][max_blocks_per_seq]; only the
+ *                 entries of pages holding keys in the window are read.
+ *   seq_lens      device int32 [num_seqs], 0 <= L <= max_blocks_per_seq *
+ *                 block_size (L = 0 writes a zero row).
+ *   out           device bf16 [num_seqs][num_q_heads][head_dim].
+ *   scale         score multiplier, usually 1/sqrt(head_dim).
+ *   num_splits    0 = pd_choose_num_splits on the current device, else S.
+ *   sliding_window  0 = off; W > 0 keeps keys j with (L-1) - j < W.
+ *   k_scale, v_scale  FP8 per-tensor scales (ignored for other forms).
+ *   workspace     device scratch of >= pd_decode_workspace_bytes(num_seqs,
+ *                 num_q_heads, head_dim, S) bytes; its contents on entry do
+ *                 not matter.
+ * ([metrale] `paged_decode_attn_splitk_{nvfp4,fp8,bf16}` +
+ * `paged_decode_attn_reduce_{nvfp4,fp8}`; [AstrAI] split-KV paged decode
+ * with o_part / ml_part and one combine kernel.)
+ * Supported: head_dim in {64, 128, 256, 512} (NVFP4: all of them);
+ * block_size in {16, 32}; num_q_heads % num_kv_heads == 0 with a group of
+ * at most 16; 1 <= S <= 1024. */
+int pd_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+              const int32_t* seq_lens, void* out, int32_t num_seqs, int32_t num_q_heads,
+              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+              int32_t max_blocks_per_seq, int64_t num_blocks, float scale, int32_t num_splits,
+              int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
+              void* workspace, size_t workspace_bytes, void* stream);
+
+/* The first half of pd_decode alone: writes the S partials (O_s normalised,
+ * m_s, l_s) of every (sequence, q head) to the workspace ([metrale]: "each
+ * block writes its partial output and softmax state to workspace"). Same
+ * arguments as pd_decode, with num_splits >= 1 required. Splits that hold
+ * no key of a sequence are not written. */
+int pd_decode_partial(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* seq_lens, int32_t num_seqs,
+                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, int32_t max_blocks_per_seq, int64_t num_blocks,
+                      float scale, int32_t num_splits, int32_t sliding_window, int32_t kv_dtype,
+                      float k_scale, float v_scale, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/* The second half of pd_decode alone: merges the partials that
+ * pd_decode_partial wrote into out, M = max_s m_s, w_s = l_s exp(m_s - M),
+ * out = bf16(sum_s w_s O_s / max(sum_s w_s, 1e-20)) ([metrale] `paged_decode
+ * _attn_reduce_fp8`: "Combine split-K partials into the BF16 output"; it
+ * reads seq_lens to know how many splits of each sequence hold keys).
+ * Arguments must match the pd_decode_partial call that filled workspace. */
+int pd_decode_combine(const void* workspace, size_t workspace_bytes, const int32_t* seq_lens,
+                      void* out, int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                      int32_t block_size, int32_t max_blocks_per_seq, int32_t num_splits,
+                      int32_t sliding_window, void* stream);
+
+/* Read (and, if reset != 0, clear) the pd_device_flag bits that kernels on
+ * the current device have raised since the last reset. Synchronises the
+ * device (cudaMemcpyFromSymbol): a debugging call, not for the hot path. */
+int pd_device_status(int32_t* flags, int32_t reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PD_H_ */

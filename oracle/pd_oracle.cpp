@@ -35,7 +35,8 @@
  *     saturate finite overflow and +-Inf to the largest finite magnitude
  *     (448 / 6). The sign of a value that rounds to zero is kept.
  *     E4M3 NaN input -> 0x7F | sign; E2M1 has no NaN, so NaN saturates to 6.
- *   - FP8 quantisation divides: code = E4M3(float(x) / scale).
+ *   - FP8 quantisation divides: code = E4M3(float(x) / scale); a NaN input
+ *     keeps its own sign (IEEE does not fix the sign of a NaN quotient).
  *   - FP8 calibration scale = amax / 448 (1.0 when amax == 0).
  *   - NVFP4 group scale = E4M3(amax / 6), amax over the 16 values with NaN
  *     skipped; a group whose decoded scale is 0 stores +0 codes; otherwise
@@ -176,6 +177,10 @@ uint8_t e2m1_code(float x) {
   return static_cast<uint8_t>(((field << 1) | man) | sign);
 }
 
+/* x / s in IEEE fp32; a NaN x is passed through unchanged so that its sign
+ * (which IEEE leaves unspecified for a NaN quotient) selects the code. */
+float quotient(float x, float s) { return std::isnan(x) ? x : x / s; }
+
 /* ---- Cache geometry (bytes). */
 int64_t page_bytes(int kv_dtype, int32_t bs, int32_t hkv, int32_t d) {
   const int64_t elems = static_cast<int64_t>(bs) * hkv * d;
@@ -279,7 +284,7 @@ int oracle_reshape_and_cache(const uint16_t* key, const uint16_t* value, uint8_t
           for (int32_t i = 0; i < head_dim; ++i) dst[i] = x[i];
         } else if (kv_dtype == KV_FP8) {
           uint8_t* dst = base + (static_cast<int64_t>(off) * num_kv_heads + h) * head_dim;
-          for (int32_t i = 0; i < head_dim; ++i) dst[i] = e4m3_code(bf16_value(x[i]) / sc);
+          for (int32_t i = 0; i < head_dim; ++i) dst[i] = e4m3_code(quotient(bf16_value(x[i]), sc));
         } else {
           uint8_t* data = base + (static_cast<int64_t>(h) * block_size + off) * (head_dim / 2);
           uint8_t* scl = base + nvfp4_data_bytes(block_size, num_kv_heads, head_dim) +
@@ -296,8 +301,8 @@ int oracle_reshape_and_cache(const uint16_t* key, const uint16_t* value, uint8_t
             for (int32_t i = 0; i < 16; i += 2) {
               uint8_t lo = 0, hi = 0;
               if (s != 0.0f) {
-                lo = e2m1_code(bf16_value(x[g * 16 + i]) / s);
-                hi = e2m1_code(bf16_value(x[g * 16 + i + 1]) / s);
+                lo = e2m1_code(quotient(bf16_value(x[g * 16 + i]), s));
+                hi = e2m1_code(quotient(bf16_value(x[g * 16 + i + 1]), s));
               }
               data[(g * 16 + i) / 2] = static_cast<uint8_t>(lo | (hi << 4));
             }

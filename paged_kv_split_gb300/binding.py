@@ -1,0 +1,247 @@
+"""Python binding of libpd.so (include/pd.h): argument marshalling only.
+
+Every function here takes torch tensors on a CUDA device, checks their
+dtypes, shapes and devices, and passes raw pointers, sizes and torch's
+current CUDA stream to the C entry point of the same name. All compute runs
+in libpd.so's kernels; there is no fallback path. Importing this module
+raises ImportError when libpd.so has not been built
+(``python -m paged_kv_split_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"{_LIB_PATH} is not built; run `python -m paged_kv_split_gb300.build` "
+                      "(or __graft_entry__.build()) on a machine with nvcc")
+
+_lib = ctypes.CDLL(_LIB_PATH)
+
+PD_OK = 0
+PD_KV_BF16, PD_KV_FP8_E4M3, PD_KV_NVFP4 = 0, 1, 2
+KV_DTYPES = {"bf16": PD_KV_BF16, "fp8": PD_KV_FP8_E4M3, "nvfp4": PD_KV_NVFP4}
+
+_P = ctypes.c_void_p
+_i32, _i64, _f32, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+
+_lib.pd_status_string.argtypes, _lib.pd_status_string.restype = [ctypes.c_int], ctypes.c_char_p
+_lib.pd_cache_bytes.argtypes, _lib.pd_cache_bytes.restype = [_i32, _i64, _i32, _i32, _i32], _sz
+_lib.pd_page_bytes.argtypes, _lib.pd_page_bytes.restype = [_i32, _i32, _i32, _i32], _sz
+_lib.pd_decode_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32]
+_lib.pd_decode_workspace_bytes.restype = _sz
+_lib.pd_choose_num_splits.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_int]
+_lib.pd_choose_num_splits.restype = ctypes.c_int
+_lib.pd_plan_num_splits.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
+_lib.pd_plan_num_splits.restype = ctypes.c_int
+_lib.pd_reshape_and_cache.argtypes = [_P, _P, _P, _P, _P, _i32, _i32, _i32, _i32, _i64, _i32,
+                                      _f32, _f32, _P]
+_lib.pd_reshape_and_cache.restype = ctypes.c_int
+_lib.pd_absmax_bf16.argtypes, _lib.pd_absmax_bf16.restype = [_P, _i64, _P, _P], ctypes.c_int
+_DECODE_ARGS = [_P, _P, _P, _P, _P, _P, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _f32, _i32,
+                _i32, _i32, _f32, _f32, _P, _sz, _P]
+_lib.pd_decode.argtypes, _lib.pd_decode.restype = _DECODE_ARGS, ctypes.c_int
+_lib.pd_decode_partial.argtypes = [_P, _P, _P, _P, _P, _i32, _i32, _i32, _i32, _i32, _i32, _i64,
+                                   _f32, _i32, _i32, _i32, _f32, _f32, _P, _sz, _P]
+_lib.pd_decode_partial.restype = ctypes.c_int
+_lib.pd_decode_combine.argtypes = [_P, _sz, _P, _P, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _P]
+_lib.pd_decode_combine.restype = ctypes.c_int
+_lib.pd_device_status.argtypes, _lib.pd_device_status.restype = [_P, _i32], ctypes.c_int
+
+
+class PdError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {pd_status_string(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libpd.so handle (for callers that want the raw C entry points)."""
+    return _lib
+
+
+def pd_status_string(status: int) -> str:
+    return _lib.pd_status_string(int(status)).decode()
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != PD_OK:
+        raise PdError(fn, rc)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(getattr(stream, "cuda_stream", stream) or 0)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, device=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t.data_ptr()
+
+
+def _dtype_code(kv_dtype) -> int:
+    return KV_DTYPES[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
+
+
+# ---- sizes ----------------------------------------------------------------
+def pd_cache_bytes(kv_dtype, num_blocks, block_size, num_kv_heads, head_dim) -> int:
+    return int(_lib.pd_cache_bytes(_dtype_code(kv_dtype), num_blocks, block_size, num_kv_heads,
+                                   head_dim))
+
+
+def pd_page_bytes(kv_dtype, block_size, num_kv_heads, head_dim) -> int:
+    return int(_lib.pd_page_bytes(_dtype_code(kv_dtype), block_size, num_kv_heads, head_dim))
+
+
+def pd_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, num_splits) -> int:
+    return int(_lib.pd_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, num_splits))
+
+
+def pd_plan_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, sliding_window,
+                       num_sms) -> int:
+    s = _lib.pd_plan_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size,
+                                sliding_window, num_sms)
+    if s < 1:
+        raise PdError("pd_plan_num_splits", -s)
+    return s
+
+
+def pd_choose_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, sliding_window,
+                         head_dim, kv_dtype, device=None) -> int:
+    dev = torch.cuda.current_device() if device is None else int(device)
+    s = _lib.pd_choose_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size,
+                                  sliding_window, head_dim, _dtype_code(kv_dtype), dev)
+    if s < 1:
+        raise PdError("pd_choose_num_splits", -s)
+    return s
+
+
+def empty_cache(kv_dtype, num_blocks, block_size, num_kv_heads, head_dim, device="cuda"):
+    """One K (or V) cache as a flat uint8 tensor of pd_cache_bytes bytes."""
+    n = pd_cache_bytes(kv_dtype, num_blocks, block_size, num_kv_heads, head_dim)
+    if n == 0:
+        raise ValueError("unsupported cache shape")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+# ---- operations -----------------------------------------------------------
+def pd_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, *, num_blocks, block_size,
+                         kv_dtype=PD_KV_BF16, k_scale=1.0, v_scale=1.0, stream=None) -> None:
+    """Write key/value (bf16 [T, Hkv, D]) into the caches at slot_mapping (int32 [T])."""
+    T, hkv, d = key.shape
+    dev = key.device
+    if value.shape != key.shape:
+        raise ValueError("key and value shapes differ")
+    if slot_mapping.shape != (T,):
+        raise ValueError("slot_mapping must be [num_tokens]")
+    rc = _lib.pd_reshape_and_cache(
+        _dev(key, "key", torch.bfloat16, dev), _dev(value, "value", torch.bfloat16, dev),
+        _dev(k_cache, "k_cache", None, dev), _dev(v_cache, "v_cache", None, dev),
+        _dev(slot_mapping, "slot_mapping", torch.int32, dev), T, hkv, d, block_size, num_blocks,
+        _dtype_code(kv_dtype), float(k_scale), float(v_scale), _stream(stream))
+    _check("pd_reshape_and_cache", rc)
+
+
+def pd_absmax_bf16(data, out_max, stream=None) -> None:
+    """Fold max |data| into out_max (float32 [1], caller-zeroed)."""
+    rc = _lib.pd_absmax_bf16(_dev(data, "data", torch.bfloat16), data.numel(),
+                             _dev(out_max, "out_max", torch.float32), _stream(stream))
+    _check("pd_absmax_bf16", rc)
+
+
+def fp8_calibrate(key, value, stream=None):
+    """Per-tensor FP8 scales (absmax / 448, 1.0 when absmax is 0) for key and value.
+
+    Runs pd_absmax_bf16 on the device, then reads the two maxima back (one
+    synchronising copy: calibration is a one-off step, not part of decode)."""
+    amax = torch.zeros(2, dtype=torch.float32, device=key.device)
+    pd_absmax_bf16(key, amax[0:1], stream)
+    pd_absmax_bf16(value, amax[1:2], stream)
+    a = amax.cpu()
+    scales = torch.where(a > 0, a / torch.tensor(448.0, dtype=torch.float32),
+                         torch.ones_like(a))
+    return float(scales[0]), float(scales[1])
+
+
+def _decode_shape(q, block_tables, seq_lens, out=None):
+    B, hq, d = q.shape
+    if block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("block_tables must be [num_seqs, max_blocks_per_seq]")
+    if seq_lens.shape != (B,):
+        raise ValueError("seq_lens must be [num_seqs]")
+    if out is not None and out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    return B, hq, d, block_tables.shape[1]
+
+
+def pd_decode(q, k_cache, v_cache, block_tables, seq_lens, out, *, num_kv_heads, block_size,
+              num_blocks, scale, num_splits=0, sliding_window=0, kv_dtype=PD_KV_BF16,
+              k_scale=1.0, v_scale=1.0, workspace=None, stream=None):
+    """One decode step (split-KV partials + combine) into out (bf16 [B, Hq, D]).
+
+    workspace: a CUDA uint8 tensor of at least pd_decode_workspace_bytes for
+    the split count used; when None, one is allocated here with torch."""
+    B, hq, d, mbs = _decode_shape(q, block_tables, seq_lens, out)
+    code = _dtype_code(kv_dtype)
+    S = num_splits
+    if workspace is None:
+        if S == 0:
+            S = pd_choose_num_splits(B, num_kv_heads, mbs, block_size, sliding_window, d, code,
+                                     q.device.index)
+        workspace = torch.empty(max(pd_decode_workspace_bytes(B, hq, d, S), 16), dtype=torch.uint8,
+                                device=q.device)
+    dev = q.device
+    rc = _lib.pd_decode(
+        _dev(q, "q", torch.bfloat16, dev), _dev(k_cache, "k_cache", None, dev),
+        _dev(v_cache, "v_cache", None, dev), _dev(block_tables, "block_tables", torch.int32, dev),
+        _dev(seq_lens, "seq_lens", torch.int32, dev), _dev(out, "out", torch.bfloat16, dev), B,
+        hq, num_kv_heads, d, block_size, mbs, num_blocks, float(scale), S, sliding_window, code,
+        float(k_scale), float(v_scale), _dev(workspace, "workspace", None, dev),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("pd_decode", rc)
+    return out
+
+
+def pd_decode_partial(q, k_cache, v_cache, block_tables, seq_lens, workspace, *, num_kv_heads,
+                      block_size, num_blocks, scale, num_splits, sliding_window=0,
+                      kv_dtype=PD_KV_BF16, k_scale=1.0, v_scale=1.0, stream=None):
+    B, hq, d, mbs = _decode_shape(q, block_tables, seq_lens)
+    dev = q.device
+    rc = _lib.pd_decode_partial(
+        _dev(q, "q", torch.bfloat16, dev), _dev(k_cache, "k_cache", None, dev),
+        _dev(v_cache, "v_cache", None, dev), _dev(block_tables, "block_tables", torch.int32, dev),
+        _dev(seq_lens, "seq_lens", torch.int32, dev), B, hq, num_kv_heads, d, block_size, mbs,
+        num_blocks, float(scale), num_splits, sliding_window, _dtype_code(kv_dtype),
+        float(k_scale), float(v_scale), _dev(workspace, "workspace", None, dev),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("pd_decode_partial", rc)
+
+
+def pd_decode_combine(workspace, seq_lens, out, *, block_size, max_blocks_per_seq, num_splits,
+                      sliding_window=0, stream=None):
+    B, hq, d = out.shape
+    dev = out.device
+    rc = _lib.pd_decode_combine(
+        _dev(workspace, "workspace", None, dev), workspace.numel() * workspace.element_size(),
+        _dev(seq_lens, "seq_lens", torch.int32, dev), _dev(out, "out", torch.bfloat16, dev), B, hq,
+        d, block_size, max_blocks_per_seq, num_splits, sliding_window, _stream(stream))
+    _check("pd_decode_combine", rc)
+
+
+def pd_device_status(reset: bool = False) -> int:
+    """pd_device_flag bits raised by kernels on the current device (synchronises)."""
+    v = ctypes.c_int32(0)
+    _check("pd_device_status", _lib.pd_device_status(ctypes.addressof(v), int(bool(reset))))
+    return int(v.value)

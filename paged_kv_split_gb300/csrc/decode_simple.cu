@@ -1,0 +1,252 @@
+// Split-KV partial (CUDA-core form) and the log-sum-exp combine.
+//
+// metrale "prefill_attn_b.rs": `paged_decode_attn_splitk_{nvfp4,fp8,bf16}` cut
+// each sequence's keys into num_splits parts, each block writing its partial
+// output and softmax state (F32 [head_dim values, m, l]) to a workspace, and
+// `paged_decode_attn_reduce_*` combine them into the BF16 output, reading
+// seq_lens. AstrAI "csrc/tests": split-KV decode with o_part / ml_part and a
+// single combine kernel; fmaf for the V accumulation; 1e-20 divide guards.
+//
+// This partial kernel is the plain form: one CTA per (sequence, kv head,
+// split) packs the whole GQA group so every K/V element is read once per kv
+// head; scores use warp reductions over head_dim; online softmax over tiles
+// of 64 keys; V accumulation in fp32 registers. Scores are kept in log2
+// units (scale * log2(e) folded into q), exponentials are exp2f.
+#include "pd_common.cuh"
+
+namespace pd {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTile = 64;
+
+// Dequantised element d of the (page, row, head) row of a cache.
+template <int FMT>
+__device__ __forceinline__ float load_kv(const uint8_t* __restrict__ cache, int64_t page, int row,
+                                         int head, int d, const DecodeArgs& a, int D, float sc) {
+  const uint8_t* base = cache + page * a.page_bytes;
+  if (FMT == PD_KV_BF16) {
+    const uint16_t* p = reinterpret_cast<const uint16_t*>(base) +
+                        (static_cast<int64_t>(row) * a.num_kv_heads + head) * D + d;
+    return bf16_to_f32(*p);
+  } else if (FMT == PD_KV_FP8_E4M3) {
+    const uint8_t* p = base + (static_cast<int64_t>(row) * a.num_kv_heads + head) * D + d;
+    return e4m3_decode(*p) * sc;
+  } else {
+    const int64_t line = static_cast<int64_t>(head) * a.block_size + row;
+    const uint8_t byte = base[line * (D / 2) + d / 2];
+    const uint32_t code = (d & 1) ? (byte >> 4) : (byte & 0xFu);
+    const float s = e4m3_decode(base[a.data_bytes + line * (D / 16) + d / 16]);
+    return e2m1_decode(code) * s;
+  }
+}
+
+template <int FMT, int D>
+__global__ void __launch_bounds__(kThreads) partial_simple_kernel(const DecodeArgs a) {
+  constexpr int kPerLane = D / 32;
+  constexpr int kAccMax = kMaxGroup * D / kThreads;
+  const int g = blockIdx.x;  // kv head
+  const int s = blockIdx.y;  // split
+  const int b = blockIdx.z;  // sequence
+  const int G = a.group;
+  const int bs = a.block_size;
+  const int L = checked_seq_len(a.seq_lens, b, a.max_blocks_per_seq, bs, a.flags);
+  const int lo = window_lo(L, a.sliding_window);
+  const int P = num_key_pages(L, a.sliding_window, bs);
+  if (s * a.chunk >= P) return;  // this split holds no key of sequence b
+  const int first_page = lo / bs + s * a.chunk;
+  const int last_page = min(lo / bs + P, first_page + a.chunk);  // exclusive
+  const int t_begin = max(lo, first_page * bs);
+  const int t_end = min(L, last_page * bs);
+
+  extern __shared__ float smem[];
+  float* qs = smem;                 // [G][D], q * scale * log2(e)
+  float* sc = qs + G * D;           // [G][kTile] scores, then probabilities
+  float* m_s = sc + G * kTile;      // [G] running max (log2 units)
+  float* l_s = m_s + kMaxGroup;     // [G] running sum
+  float* alpha_s = l_s + kMaxGroup; // [G] rescale factor of the current tile
+
+  const uint16_t* qg = a.q + (static_cast<int64_t>(b) * a.num_q_heads + g * G) * D;
+  for (int i = threadIdx.x; i < G * D; i += kThreads) qs[i] = bf16_to_f32(qg[i]) * a.scale_log2;
+  if (threadIdx.x < G) {
+    m_s[threadIdx.x] = -INFINITY;
+    l_s[threadIdx.x] = 0.0f;
+  }
+  float acc[kAccMax];
+#pragma unroll
+  for (int k = 0; k < kAccMax; ++k) acc[k] = 0.0f;
+  __syncthreads();
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
+
+  for (int t0 = t_begin; t0 < t_end; t0 += kTile) {
+    const int n = min(kTile, t_end - t0);
+    // scores: one warp per key, lanes over head_dim
+    for (int tt = warp; tt < n; tt += kWarps) {
+      const int j = t0 + tt;
+      const int64_t page = bt[j / bs];
+      const bool ok = page >= 0 && page < a.num_blocks;
+      float kv[kPerLane];
+#pragma unroll
+      for (int i = 0; i < kPerLane; ++i)
+        kv[i] = ok ? load_kv<FMT>(a.k_cache, page, j % bs, g, lane + 32 * i, a, D, a.k_scale)
+                   : 0.0f;
+      for (int h = 0; h < G; ++h) {
+        float part = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) part = fmaf(qs[h * D + lane + 32 * i], kv[i], part);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
+        if (lane == 0) sc[h * kTile + tt] = ok ? part : -INFINITY;
+      }
+      if (!ok && lane == 0) atomicOr(a.flags, PD_DEV_BAD_PAGE);
+    }
+    __syncthreads();
+    // online softmax update, one thread per q head
+    if (threadIdx.x < G) {
+      const int h = threadIdx.x;
+      float mx = m_s[h];
+      for (int tt = 0; tt < n; ++tt) mx = fmaxf(mx, sc[h * kTile + tt]);
+      const float alpha = (mx == -INFINITY) ? 1.0f : exp2f(m_s[h] - mx);
+      float l = l_s[h] * alpha;
+      for (int tt = 0; tt < n; ++tt) {
+        const float p = (mx == -INFINITY) ? 0.0f : exp2f(sc[h * kTile + tt] - mx);
+        sc[h * kTile + tt] = p;
+        l += p;
+      }
+      m_s[h] = mx;
+      l_s[h] = l;
+      alpha_s[h] = alpha;
+    }
+    __syncthreads();
+    // acc[h][d] = alpha * acc + sum_t p[h][t] * v_t[d]
+#pragma unroll
+    for (int k = 0; k < kAccMax; ++k) {
+      const int e = threadIdx.x + k * kThreads;
+      if (e < G * D) {
+        const int h = e / D;
+        const int d = e % D;
+        float v = acc[k] * alpha_s[h];
+        for (int tt = 0; tt < n; ++tt) {
+          const int j = t0 + tt;
+          const int64_t page = bt[j / bs];
+          if (page < 0 || page >= a.num_blocks) continue;
+          const float vv = load_kv<FMT>(a.v_cache, page, j % bs, g, d, a, D, a.v_scale);
+          v = fmaf(sc[h * kTile + tt], vv, v);
+        }
+        acc[k] = v;
+      }
+    }
+    __syncthreads();
+  }
+  // write the normalised partial and its (m, l)
+  const int64_t row0 = (static_cast<int64_t>(b) * a.num_q_heads + g * G) * a.num_splits + s;
+#pragma unroll
+  for (int k = 0; k < kAccMax; ++k) {
+    const int e = threadIdx.x + k * kThreads;
+    if (e < G * D) {
+      const int h = e / D;
+      const int d = e % D;
+      const float l = l_s[h];
+      a.ws_o[(row0 + static_cast<int64_t>(h) * a.num_splits) * D + d] =
+          acc[k] / fmaxf(l, 1e-20f);
+    }
+  }
+  if (threadIdx.x < G) {
+    const int h = threadIdx.x;
+    a.ws_ml[row0 + static_cast<int64_t>(h) * a.num_splits] = make_float2(m_s[h], l_s[h]);
+  }
+}
+
+// Combine: one CTA of D/4 threads per (q head, sequence); each thread owns
+// 4 consecutive output elements.
+template <int D>
+__global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
+  const int h = blockIdx.x;
+  const int b = blockIdx.y;
+  const int S = a.num_splits;
+  int L = a.seq_lens[b];
+  const int cap = a.max_blocks_per_seq * a.block_size;
+  L = L < 0 ? 0 : (L > cap ? cap : L);
+  const int P = num_key_pages(L, a.sliding_window, a.block_size);
+  const int n = min((P + a.chunk - 1) / a.chunk, S);  // splits holding keys
+  const int64_t row0 = (static_cast<int64_t>(b) * a.num_q_heads + h) * S;
+  float M = -INFINITY;
+  for (int s = 0; s < n; ++s) M = fmaxf(M, a.ws_ml[row0 + s].x);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.0f;
+  const int d = threadIdx.x * 4;
+  for (int s = 0; s < n; ++s) {
+    const float2 ml = a.ws_ml[row0 + s];
+    const float w = (M == -INFINITY) ? 0.0f : ml.y * exp2f(ml.x - M);
+    const float4 o = *reinterpret_cast<const float4*>(a.ws_o + (row0 + s) * D + d);
+    wsum += w;
+    acc.x = fmaf(w, o.x, acc.x);
+    acc.y = fmaf(w, o.y, acc.y);
+    acc.z = fmaf(w, o.z, acc.z);
+    acc.w = fmaf(w, o.w, acc.w);
+  }
+  const float inv = 1.0f / fmaxf(wsum, 1e-20f);
+  const uint32_t lo01 = static_cast<uint32_t>(f32_to_bf16(acc.x * inv)) |
+                        (static_cast<uint32_t>(f32_to_bf16(acc.y * inv)) << 16);
+  const uint32_t lo23 = static_cast<uint32_t>(f32_to_bf16(acc.z * inv)) |
+                        (static_cast<uint32_t>(f32_to_bf16(acc.w * inv)) << 16);
+  *reinterpret_cast<uint2*>(a.out + (static_cast<int64_t>(b) * a.num_q_heads + h) * D + d) =
+      make_uint2(lo01, lo23);
+}
+
+template <int FMT, int D>
+cudaError_t launch_simple(const DecodeArgs& a, cudaStream_t st) {
+  const size_t smem = (static_cast<size_t>(a.group) * D + a.group * kTile + 3 * kMaxGroup) *
+                      sizeof(float);
+  auto kern = partial_simple_kernel<FMT, D>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  const dim3 grid(a.num_kv_heads, a.num_splits, a.num_seqs);
+  kern<<<grid, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int FMT>
+cudaError_t launch_simple_fmt(const DecodeArgs& a, int D, cudaStream_t st) {
+  switch (D) {
+    case 64: return launch_simple<FMT, 64>(a, st);
+    case 128: return launch_simple<FMT, 128>(a, st);
+    case 256: return launch_simple<FMT, 256>(a, st);
+    case 512: return launch_simple<FMT, 512>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_partial(const DecodeArgs& a, int head_dim, int kv_dtype,
+                                  cudaStream_t st) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  switch (kv_dtype) {
+    case PD_KV_BF16: return launch_simple_fmt<PD_KV_BF16>(a, head_dim, st);
+    case PD_KV_FP8_E4M3: return launch_simple_fmt<PD_KV_FP8_E4M3>(a, head_dim, st);
+    default: return launch_simple_fmt<PD_KV_NVFP4>(a, head_dim, st);
+  }
+}
+
+cudaError_t launch_decode_combine(const CombineArgs& a, int head_dim, cudaStream_t st) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  const dim3 grid(a.num_q_heads, a.num_seqs);
+  switch (head_dim) {
+    case 64: combine_kernel<64><<<grid, 16, 0, st>>>(a); break;
+    case 128: combine_kernel<128><<<grid, 32, 0, st>>>(a); break;
+    case 256: combine_kernel<256><<<grid, 64, 0, st>>>(a); break;
+    case 512: combine_kernel<512><<<grid, 128, 0, st>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pd

@@ -1,0 +1,314 @@
+// The C ABI of libpd.so (declared in include/pd.h): argument validation, the
+// split planner and dispatch to the kernels. Nothing here allocates device
+// memory or synchronises, except pd_device_status (a debugging read).
+#include <math.h>
+
+#include <mutex>
+
+#include "pd_common.cuh"
+
+namespace pd {
+namespace {
+
+// Device status word (pd_device_flag bits); kernels get its device address.
+__device__ int g_device_flags;
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 1024;
+
+struct DeviceInfo {
+  std::once_flag once;
+  int num_sms = 0;
+  int* flags = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+DeviceInfo g_devices[kMaxDevices];
+
+// SM count and status-word address of the current device (looked up once).
+cudaError_t current_device(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  DeviceInfo& d = g_devices[dev];
+  std::call_once(d.once, [&d, dev]() {
+    d.err = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (d.err == cudaSuccess)
+      d.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.flags), g_device_flags);
+  });
+  *out = &d;
+  return d.err;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool dev_ptr_ok(const void* p) { return p != nullptr && aligned16(p); }
+bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256 || d == 512; }
+bool block_size_ok(int bs) { return bs == 16 || bs == 32; }
+bool dtype_ok(int t) { return t == PD_KV_BF16 || t == PD_KV_FP8_E4M3 || t == PD_KV_NVFP4; }
+bool scale_ok(float s) { return isfinite(s) && s > 0.0f; }
+
+struct DecodeShape {
+  int B, Hq, Hkv, D, bs, mbs, S, W, kv_dtype;
+  int64_t nb;
+};
+
+// Shared checks of pd_decode / pd_decode_partial (S already resolved).
+int check_decode(const DecodeShape& s, const void* q, const void* kc, const void* vc,
+                 const int32_t* bt, const int32_t* lens, float k_scale, float v_scale,
+                 const void* ws, size_t ws_bytes) {
+  if (s.B < 0 || s.B > 65535) return PD_ERR_INVALID_ARG;
+  if (s.Hkv <= 0 || s.Hq <= 0 || s.Hq % s.Hkv != 0) return PD_ERR_INVALID_ARG;
+  if (s.Hq / s.Hkv > kMaxGroup) return PD_ERR_UNSUPPORTED;
+  if (!head_dim_ok(s.D) || !block_size_ok(s.bs)) return PD_ERR_UNSUPPORTED;
+  if (!dtype_ok(s.kv_dtype)) return PD_ERR_UNSUPPORTED;
+  if (s.mbs <= 0 || s.nb <= 0 || s.W < 0) return PD_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(s.mbs) * s.bs > (int64_t{1} << 30)) return PD_ERR_INVALID_ARG;
+  if (s.S < 1 || s.S > kMaxSplits) return PD_ERR_INVALID_ARG;
+  if (s.kv_dtype == PD_KV_FP8_E4M3 && !(scale_ok(k_scale) && scale_ok(v_scale)))
+    return PD_ERR_INVALID_ARG;
+  if (s.B == 0) return PD_OK;
+  if (!dev_ptr_ok(q) || !dev_ptr_ok(kc) || !dev_ptr_ok(vc) || !dev_ptr_ok(bt) ||
+      !dev_ptr_ok(lens) || !dev_ptr_ok(ws))
+    return PD_ERR_INVALID_ARG;
+  if (ws_bytes < ws_total_bytes(s.B, s.Hq, s.D, s.S)) return PD_ERR_WORKSPACE_TOO_SMALL;
+  return PD_OK;
+}
+
+DecodeArgs make_decode_args(const DecodeShape& s, const void* q, const void* kc, const void* vc,
+                            const int32_t* bt, const int32_t* lens, float scale, float k_scale,
+                            float v_scale, void* ws, int* flags) {
+  DecodeArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k_cache = static_cast<const uint8_t*>(kc);
+  a.v_cache = static_cast<const uint8_t*>(vc);
+  a.block_tables = bt;
+  a.seq_lens = lens;
+  a.ws_o = static_cast<float*>(ws);
+  a.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + ws_o_bytes(s.B, s.Hq, s.D, s.S));
+  a.flags = flags;
+  a.num_blocks = s.nb;
+  a.page_bytes = page_bytes_of(s.kv_dtype, s.bs, s.Hkv, s.D);
+  a.data_bytes = nvfp4_data_bytes(s.bs, s.Hkv, s.D);
+  a.num_seqs = s.B;
+  a.num_q_heads = s.Hq;
+  a.num_kv_heads = s.Hkv;
+  a.group = s.Hq / s.Hkv;
+  a.block_size = s.bs;
+  a.max_blocks_per_seq = s.mbs;
+  a.num_splits = s.S;
+  a.chunk = chunk_pages(page_span_max(s.mbs, s.bs, s.W), s.S);
+  a.sliding_window = s.W;
+  a.scale_log2 = scale * kLog2e;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  return a;
+}
+
+CombineArgs make_combine_args(int B, int Hq, int D, int bs, int mbs, int S, int W, const void* ws,
+                              const int32_t* lens, void* out) {
+  CombineArgs c;
+  c.ws_o = static_cast<const float*>(ws);
+  c.ws_ml = reinterpret_cast<const float2*>(static_cast<const char*>(ws) + ws_o_bytes(B, Hq, D, S));
+  c.seq_lens = lens;
+  c.out = static_cast<uint16_t*>(out);
+  c.num_seqs = B;
+  c.num_q_heads = Hq;
+  c.block_size = bs;
+  c.max_blocks_per_seq = mbs;
+  c.num_splits = S;
+  c.chunk = chunk_pages(page_span_max(mbs, bs, W), S);
+  c.sliding_window = W;
+  return c;
+}
+
+int plan_splits(int B, int Hkv, int mbs, int bs, int W, int num_sms) {
+  // Work units without splitting: one CTA per (sequence, kv head). Aim for
+  // a few resident CTAs per SM, but keep at least ~4 pages of 16 (64 keys)
+  // per split so the partial write stays small against the KV read.
+  const int span = page_span_max(mbs, bs, W);
+  const int64_t units = static_cast<int64_t>(B > 0 ? B : 1) * (Hkv > 0 ? Hkv : 1);
+  const int64_t target = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 4;
+  int64_t S = (target + units - 1) / units;
+  const int64_t min_pages = (bs >= 32) ? 2 : 4;
+  const int64_t cap = (span + min_pages - 1) / min_pages;
+  if (S > cap) S = cap;
+  if (S < 1) S = 1;
+  if (S > kMaxSplits) S = kMaxSplits;
+  return static_cast<int>(S);
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? PD_OK : PD_ERR_CUDA; }
+
+}  // namespace
+}  // namespace pd
+
+using namespace pd;
+
+extern "C" {
+
+const char* pd_status_string(int status) {
+  switch (status) {
+    case PD_OK: return "PD_OK";
+    case PD_ERR_INVALID_ARG: return "PD_ERR_INVALID_ARG: invalid argument";
+    case PD_ERR_UNSUPPORTED: return "PD_ERR_UNSUPPORTED: unsupported shape or dtype";
+    case PD_ERR_WORKSPACE_TOO_SMALL: return "PD_ERR_WORKSPACE_TOO_SMALL: workspace too small";
+    case PD_ERR_CUDA: return "PD_ERR_CUDA: CUDA runtime error";
+    default: return "unknown pd status";
+  }
+}
+
+size_t pd_page_bytes(int32_t kv_dtype, int32_t block_size, int32_t num_kv_heads,
+                     int32_t head_dim) {
+  if (!dtype_ok(kv_dtype) || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
+  if (kv_dtype == PD_KV_NVFP4 && head_dim % 16 != 0) return 0;
+  return static_cast<size_t>(page_bytes_of(kv_dtype, block_size, num_kv_heads, head_dim));
+}
+
+size_t pd_cache_bytes(int32_t kv_dtype, int64_t num_blocks, int32_t block_size,
+                      int32_t num_kv_heads, int32_t head_dim) {
+  if (num_blocks < 0) return 0;
+  return static_cast<size_t>(num_blocks) * pd_page_bytes(kv_dtype, block_size, num_kv_heads,
+                                                         head_dim);
+}
+
+size_t pd_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                 int32_t num_splits) {
+  if (num_seqs < 0 || num_q_heads < 0 || head_dim < 0 || num_splits < 0) return 0;
+  return ws_total_bytes(num_seqs, num_q_heads, head_dim, num_splits);
+}
+
+int pd_plan_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_blocks_per_seq,
+                       int32_t block_size, int32_t sliding_window, int32_t num_sms) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 ||
+      sliding_window < 0 || num_sms <= 0)
+    return -PD_ERR_INVALID_ARG;
+  return plan_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, sliding_window,
+                     num_sms);
+}
+
+int pd_choose_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_blocks_per_seq,
+                         int32_t block_size, int32_t sliding_window, int32_t head_dim,
+                         int32_t kv_dtype, int device) {
+  (void)head_dim;
+  (void)kv_dtype;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+    return -PD_ERR_CUDA;
+  return pd_plan_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size,
+                            sliding_window, sms);
+}
+
+int pd_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                         const int32_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                         int32_t kv_dtype, float k_scale, float v_scale, void* stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PD_ERR_INVALID_ARG;
+  if (!head_dim_ok(head_dim) || !block_size_ok(block_size) || !dtype_ok(kv_dtype))
+    return PD_ERR_UNSUPPORTED;
+  if (kv_dtype == PD_KV_FP8_E4M3 && !(scale_ok(k_scale) && scale_ok(v_scale)))
+    return PD_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PD_OK;
+  if (!dev_ptr_ok(key) || !dev_ptr_ok(value) || !dev_ptr_ok(k_cache) || !dev_ptr_ok(v_cache) ||
+      !dev_ptr_ok(slot_mapping))
+    return PD_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if (current_device(&dev) != cudaSuccess) return PD_ERR_CUDA;
+  return cuda_status(launch_reshape_and_cache(
+      static_cast<const uint16_t*>(key), static_cast<const uint16_t*>(value),
+      static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), slot_mapping, num_tokens,
+      num_kv_heads, head_dim, block_size, num_blocks, kv_dtype, k_scale, v_scale, dev->flags,
+      static_cast<cudaStream_t>(stream)));
+}
+
+int pd_absmax_bf16(const void* data, int64_t n, float* out_max, void* stream) {
+  if (n < 0) return PD_ERR_INVALID_ARG;
+  if (n == 0) return PD_OK;
+  if (!dev_ptr_ok(data) || out_max == nullptr || (reinterpret_cast<uintptr_t>(out_max) & 3u))
+    return PD_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if (current_device(&dev) != cudaSuccess) return PD_ERR_CUDA;
+  return cuda_status(launch_absmax(static_cast<const uint16_t*>(data), n, out_max, dev->num_sms,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+int pd_decode_partial(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* seq_lens, int32_t num_seqs,
+                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, int32_t max_blocks_per_seq, int64_t num_blocks,
+                      float scale, int32_t num_splits, int32_t sliding_window, int32_t kv_dtype,
+                      float k_scale, float v_scale, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                      max_blocks_per_seq, num_splits, sliding_window, kv_dtype, num_blocks};
+  const int rc = check_decode(s, q, k_cache, v_cache, block_tables, seq_lens, k_scale, v_scale,
+                              workspace, workspace_bytes);
+  if (rc != PD_OK || num_seqs == 0) return rc;
+  if (!isfinite(scale)) return PD_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if (current_device(&dev) != cudaSuccess) return PD_ERR_CUDA;
+  const DecodeArgs a = make_decode_args(s, q, k_cache, v_cache, block_tables, seq_lens, scale,
+                                        k_scale, v_scale, workspace, dev->flags);
+  return cuda_status(launch_decode_partial(a, head_dim, kv_dtype,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+int pd_decode_combine(const void* workspace, size_t workspace_bytes, const int32_t* seq_lens,
+                      void* out, int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                      int32_t block_size, int32_t max_blocks_per_seq, int32_t num_splits,
+                      int32_t sliding_window, void* stream) {
+  if (num_seqs < 0 || num_seqs > 65535 || num_q_heads <= 0 || max_blocks_per_seq <= 0 ||
+      sliding_window < 0 || num_splits < 1 || num_splits > kMaxSplits)
+    return PD_ERR_INVALID_ARG;
+  if (!head_dim_ok(head_dim) || !block_size_ok(block_size)) return PD_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PD_OK;
+  if (!dev_ptr_ok(workspace) || !dev_ptr_ok(seq_lens) || !dev_ptr_ok(out))
+    return PD_ERR_INVALID_ARG;
+  if (workspace_bytes < ws_total_bytes(num_seqs, num_q_heads, head_dim, num_splits))
+    return PD_ERR_WORKSPACE_TOO_SMALL;
+  const CombineArgs c = make_combine_args(num_seqs, num_q_heads, head_dim, block_size,
+                                          max_blocks_per_seq, num_splits, sliding_window,
+                                          workspace, seq_lens, out);
+  return cuda_status(launch_decode_combine(c, head_dim, static_cast<cudaStream_t>(stream)));
+}
+
+int pd_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+              const int32_t* seq_lens, void* out, int32_t num_seqs, int32_t num_q_heads,
+              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+              int32_t max_blocks_per_seq, int64_t num_blocks, float scale, int32_t num_splits,
+              int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
+              void* workspace, size_t workspace_bytes, void* stream) {
+  if (num_splits < 0 || num_splits > kMaxSplits) return PD_ERR_INVALID_ARG;
+  if (num_seqs > 0 && !dev_ptr_ok(out)) return PD_ERR_INVALID_ARG;
+  int S = num_splits;
+  if (S == 0) {
+    DeviceInfo* dev = nullptr;
+    if (current_device(&dev) != cudaSuccess) return PD_ERR_CUDA;
+    if (num_kv_heads <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 || sliding_window < 0)
+      return PD_ERR_INVALID_ARG;
+    S = plan_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, sliding_window,
+                    dev->num_sms);
+  }
+  int rc = pd_decode_partial(q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_q_heads,
+                             num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+                             scale, S, sliding_window, kv_dtype, k_scale, v_scale, workspace,
+                             workspace_bytes, stream);
+  if (rc != PD_OK || num_seqs == 0) return rc;
+  return pd_decode_combine(workspace, workspace_bytes, seq_lens, out, num_seqs, num_q_heads,
+                           head_dim, block_size, max_blocks_per_seq, S, sliding_window, stream);
+}
+
+int pd_device_status(int32_t* flags, int32_t reset) {
+  if (flags == nullptr) return PD_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if (current_device(&dev) != cudaSuccess) return PD_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_flags, sizeof(int)) != cudaSuccess) return PD_ERR_CUDA;
+  *flags = v;
+  if (reset) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_flags, &zero, sizeof(int)) != cudaSuccess) return PD_ERR_CUDA;
+  }
+  return PD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,137 @@
+"""libpd.so loads and exports exactly the entry points include/pd.h declares,
+and its host-only logic (sizes, split planning, argument validation) behaves
+as documented. CPU only: nothing here launches a kernel."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "pd.h")
+
+
+@pytest.fixture(scope="module")
+def pdlib():
+    from paged_kv_split_gb300 import build
+    path = build.build()
+    L = ctypes.CDLL(path)
+    return path, L
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pd_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("pd_reshape_and_cache", "pd_decode", "pd_decode_partial",
+                     "pd_decode_combine", "pd_absmax_bf16", "pd_decode_workspace_bytes",
+                     "pd_cache_bytes", "pd_choose_num_splits", "pd_status_string"):
+        assert required in names
+
+
+def test_exports_match_header(pdlib):
+    path, _ = pdlib
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = sorted({m.group(1) for m in re.finditer(r"\sT\s+(pd_[a-z0-9_]+)$", out, re.M)})
+    assert exported == declared_functions()
+
+
+def test_cache_and_workspace_sizes(pdlib):
+    _, L = pdlib
+    L.pd_cache_bytes.restype = ctypes.c_size_t
+    L.pd_cache_bytes.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                 ctypes.c_int32]
+    L.pd_decode_workspace_bytes.restype = ctypes.c_size_t
+    L.pd_decode_workspace_bytes.argtypes = [ctypes.c_int32] * 4
+    import oracle
+    orc = oracle.get()
+    for dt in (0, 1, 2):
+        for bs in (16, 32):
+            for h, d in ((2, 64), (8, 128), (4, 256), (2, 512), (1, 64)):
+                assert L.pd_cache_bytes(dt, 37, bs, h, d) == orc.cache_bytes(dt, 37, bs, h, d)
+    assert L.pd_cache_bytes(9, 1, 16, 1, 64) == 0
+    ws = L.pd_decode_workspace_bytes(32, 32, 128, 8)
+    assert ws >= 32 * 32 * 8 * (128 + 2) * 4
+
+
+def test_split_planner(pdlib):
+    _, L = pdlib
+    L.pd_plan_num_splits.argtypes = [ctypes.c_int32] * 6
+    # few work units -> more splits, bounded by the pages available
+    s_b1 = L.pd_plan_num_splits(1, 8, 1024, 32, 0, 152)
+    s_b64 = L.pd_plan_num_splits(64, 8, 1024, 16, 0, 152)
+    assert s_b1 > s_b64 >= 1
+    assert L.pd_plan_num_splits(1, 1, 1, 16, 0, 152) == 1
+    # a window bounds the pages any split can see
+    assert L.pd_plan_num_splits(1, 4, 1024, 16, 64, 152) <= 2
+    assert L.pd_plan_num_splits(1, 8, 10, 16, 0, 0) < 0
+
+
+def test_status_strings(pdlib):
+    _, L = pdlib
+    L.pd_status_string.restype = ctypes.c_char_p
+    assert L.pd_status_string(0) == b"PD_OK"
+    for s in (1, 2, 3, 4):
+        assert L.pd_status_string(s).startswith(b"PD_ERR_")
+    assert L.pd_status_string(77) == b"unknown pd status"
+
+
+def _decode_partial(L, **kw):
+    args = dict(q=0x1000, k=0x2000, v=0x3000, bt=0x4000, lens=0x5000, B=2, Hq=8, Hkv=2, D=128,
+                bs=16, mbs=4, nb=8, scale=0.1, S=2, W=0, dt=0, ks=1.0, vs=1.0, ws=0x6000,
+                ws_bytes=1 << 20)
+    args.update(kw)
+    f = L.pd_decode_partial
+    P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    f.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, f32, i32, i32, i32, f32, f32, P,
+                  ctypes.c_size_t, P]
+    a = args
+    return f(a["q"], a["k"], a["v"], a["bt"], a["lens"], a["B"], a["Hq"], a["Hkv"], a["D"],
+             a["bs"], a["mbs"], a["nb"], a["scale"], a["S"], a["W"], a["dt"], a["ks"], a["vs"],
+             a["ws"], a["ws_bytes"], None)
+
+
+def test_validation_rejects_before_any_launch(pdlib):
+    """Every case below is refused on the host (the pointers are never touched)."""
+    _, L = pdlib
+    assert _decode_partial(L, Hq=6, Hkv=4) == 1            # GQA ratio not integral
+    assert _decode_partial(L, Hq=34, Hkv=2) == 2           # group of 17 > 16
+    assert _decode_partial(L, D=96) == 2                   # head_dim not built
+    assert _decode_partial(L, bs=8) == 2                   # block size not built
+    assert _decode_partial(L, dt=5) == 2                   # unknown cache form
+    assert _decode_partial(L, S=0) == 1                    # partial needs S >= 1
+    assert _decode_partial(L, S=2000) == 1                 # too many splits
+    assert _decode_partial(L, W=-1) == 1                   # negative window
+    assert _decode_partial(L, q=0x1004) == 1               # misaligned pointer
+    assert _decode_partial(L, k=0) == 1                    # null pointer
+    assert _decode_partial(L, dt=1, ks=0.0) == 1           # FP8 needs a positive scale
+    assert _decode_partial(L, dt=1, vs=float("nan")) == 1
+    assert _decode_partial(L, ws_bytes=100) == 3           # workspace too small
+
+
+def test_reshape_and_cache_validation(pdlib):
+    _, L = pdlib
+    f = L.pd_reshape_and_cache
+    P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    f.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i64, i32, f32, f32, P]
+    ok = dict(k=0x1000, v=0x2000, kc=0x3000, vc=0x4000, sl=0x5000, T=4, H=2, D=64, bs=16, nb=4,
+              dt=0, ks=1.0, vs=1.0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["k"], a["v"], a["kc"], a["vc"], a["sl"], a["T"], a["H"], a["D"], a["bs"],
+                 a["nb"], a["dt"], a["ks"], a["vs"], None)
+    assert call(T=0) == 0                                   # nothing to do, no launch
+    assert call(D=48) == 2
+    assert call(bs=64) == 2
+    assert call(T=-1) == 1
+    assert call(kc=0x3001) == 1
+    assert call(dt=1, ks=-1.0) == 1
+    assert call(nb=0) == 1
