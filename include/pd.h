@@ -193,6 +193,37 @@ int pd_decode_combine(const void* workspace, size_t workspace_bytes, const int32
                       int32_t block_size, int32_t max_blocks_per_seq, int32_t num_splits,
                       int32_t sliding_window, void* stream);
 
+/* Size of the workspace array that pd_decode_static_ws uses (8 MiB). */
+#define PD_STATIC_WORKSPACE_BYTES (8u << 20)
+
+/* pd_decode for callers that cannot allocate device memory. None of the
+ * three pages has a counterpart of this call: it exists for code that only
+ * receives its input and output buffers - an operator running inside another
+ * runtime that owns all device memory, or a caller with a fixed memory budget
+ * - and so has no way to provide pd_decode's workspace.
+ * Arguments and results are those of pd_decode without `workspace` and
+ * `workspace_bytes`: the split partials go to a fixed array of
+ * PD_STATIC_WORKSPACE_BYTES that libpd.so reserves on every device that loads
+ * it, for the life of the process.
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library
+ *     call. The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     outside any stream capture.
+ *   - Returns PD_ERR_WORKSPACE_TOO_SMALL when pd_decode_workspace_bytes for
+ *     the split count (num_splits, or the automatic choice when 0) exceeds
+ *     PD_STATIC_WORKSPACE_BYTES.
+ *   - All calls on a device share the one array and it keeps the previous
+ *     call's contents (nothing in it needs to start at zero). Calls whose
+ *     work overlaps on the GPU - on different streams, or from different
+ *     host threads - race on it: serialise them. */
+int pd_decode_static_ws(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, const int32_t* seq_lens, void* out,
+                        int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                        int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
+                        int64_t num_blocks, float scale, int32_t num_splits,
+                        int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
+                        void* stream);
+
 /* Read (and, if reset != 0, clear) the pd_device_flag bits that kernels on
  * the current device have raised since the last reset. Synchronises the
  * device (cudaMemcpyFromSymbol): a debugging call, not for the hot path. */
