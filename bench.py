@@ -35,7 +35,7 @@ sys.path.insert(0, ROOT)
 METRIC = "decode µs/step and KV-read HBM GB/s (% of GB300 peak) at 1 GPU"
 ELEM_BYTES = {0: 2.0, 1: 1.0, 2: 0.5625}
 DTYPE_NAME = {0: "bf16", 1: "fp8_e4m3", 2: "nvfp4"}
-PARTIAL_KERNEL_SRC = ["paged_kv_split_gb300/csrc/decode_simple.cu",
+PARTIAL_KERNEL_SRC = ["paged_kv_split_gb300/csrc/decode_mma.cu",
                       "paged_kv_split_gb300/csrc/pd_common.cuh"]
 
 

@@ -71,7 +71,8 @@ enum pd_kv_dtype { PD_KV_BF16 = 0, PD_KV_FP8_E4M3 = 1, PD_KV_NVFP4 = 2 };
 enum pd_device_flag {
   PD_DEV_BAD_PAGE = 1,    /* a block_tables entry was < 0 or >= num_blocks: page skipped */
   PD_DEV_BAD_SEQ_LEN = 2, /* seq_lens[b] < 0 or > max_blocks_per_seq*block_size: clamped */
-  PD_DEV_BAD_SLOT = 4     /* slot_mapping[t] >= num_blocks*block_size: token skipped */
+  PD_DEV_BAD_SLOT = 4,    /* slot_mapping[t] >= num_blocks*block_size: token skipped */
+  PD_DEV_TIMEOUT = 8      /* a bounded wait inside a kernel gave up: that output is invalid */
 };
 
 /* Human-readable name of a pd_status value (static string, never NULL). */

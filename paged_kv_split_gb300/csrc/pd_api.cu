@@ -2,6 +2,8 @@
 // split planner and dispatch to the kernels. Nothing here allocates device
 // memory or synchronises, except pd_device_status (a debugging read).
 #include <math.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -63,6 +65,7 @@ int check_decode(const DecodeShape& s, const void* q, const void* kc, const void
   if (!dtype_ok(s.kv_dtype)) return PD_ERR_UNSUPPORTED;
   if (s.mbs <= 0 || s.nb <= 0 || s.W < 0) return PD_ERR_INVALID_ARG;
   if (static_cast<int64_t>(s.mbs) * s.bs > (int64_t{1} << 30)) return PD_ERR_INVALID_ARG;
+  if (s.nb * s.bs > INT32_MAX) return PD_ERR_INVALID_ARG;  // pool rows are int32 coordinates
   if (s.S < 1 || s.S > kMaxSplits) return PD_ERR_INVALID_ARG;
   if (s.kv_dtype == PD_KV_FP8_E4M3 && !(scale_ok(k_scale) && scale_ok(v_scale)))
     return PD_ERR_INVALID_ARG;
@@ -138,6 +141,16 @@ int plan_splits(int B, int Hkv, int mbs, int bs, int W, int num_sms) {
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? PD_OK : PD_ERR_CUDA; }
+
+// The tensor-core partial kernel runs by default; PD_PARTIAL_KERNEL=simple
+// selects the CUDA-core kernel instead (kept as an independent cross-check).
+bool use_simple_partial() {
+  static const bool simple = [] {
+    const char* v = getenv("PD_PARTIAL_KERNEL");
+    return v != nullptr && strcmp(v, "simple") == 0;
+  }();
+  return simple;
+}
 
 }  // namespace
 }  // namespace pd
@@ -248,8 +261,9 @@ int pd_decode_partial(const void* q, const void* k_cache, const void* v_cache,
   if (current_device(&dev) != cudaSuccess) return PD_ERR_CUDA;
   const DecodeArgs a = make_decode_args(s, q, k_cache, v_cache, block_tables, seq_lens, scale,
                                         k_scale, v_scale, workspace, dev->flags);
-  return cuda_status(launch_decode_partial(a, head_dim, kv_dtype,
-                                           static_cast<cudaStream_t>(stream)));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return cuda_status(use_simple_partial() ? launch_decode_partial(a, head_dim, kv_dtype, st)
+                                          : launch_decode_partial_mma(a, head_dim, kv_dtype, st));
 }
 
 int pd_decode_combine(const void* workspace, size_t workspace_bytes, const int32_t* seq_lens,

@@ -182,5 +182,7 @@ cudaError_t launch_absmax(const uint16_t* data, int64_t n, float* out, int num_s
                           cudaStream_t st);
 cudaError_t launch_decode_partial(const DecodeArgs& a, int head_dim, int kv_dtype,
                                   cudaStream_t st);
+cudaError_t launch_decode_partial_mma(const DecodeArgs& a, int head_dim, int kv_dtype,
+                                      cudaStream_t st);
 cudaError_t launch_decode_combine(const CombineArgs& a, int head_dim, cudaStream_t st);
 }  // namespace pd

@@ -2,6 +2,8 @@
 the binding) and through the oracle on the same inputs, and compare."""
 from __future__ import annotations
 
+import json
+import os
 from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
@@ -107,6 +109,12 @@ def assert_close(gpu_bits, ref_bits, atol=ATOL, rtol=RTOL, what=""):
     err = np.abs(g - r)
     bound = atol + rtol * np.abs(r)
     bad = err > bound
+    log = os.environ.get("PD_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"case": what, "n": int(err.size), "max_abs_err": float(err.max()),
+                                "max_err_over_bound": float((err / bound).max()),
+                                "max_abs_ref": float(np.abs(r).max())}) + "\n")
     if bad.any():
         i = np.argwhere(bad)[0]
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} outside tolerance; first at "

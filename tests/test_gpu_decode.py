@@ -81,12 +81,15 @@ def test_small_parity(orc, kv_dtype, spec):
 def test_split_independence(orc):
     case = inputs.make_case("splits", [2000, 777, 64], 32, 8, 128, 16, seed=5)
     outs, _ = run_parity(orc, case, 0, [1, 2, 4, 16, 64])
-    base = U.bf16_bits_to_f32(outs[1])
+    base = U.bf16_bits_to_f32(outs[1]).astype(np.float64)
+    # The split count changes only rounding (summation order, the bf16 rounding
+    # of the softmax weights relative to each split's running max), whose size
+    # follows the scale of the whole output row, not of each element.
+    rms = np.sqrt(np.mean(base ** 2, axis=-1, keepdims=True))
     for S, o in outs.items():
         d = np.abs(U.bf16_bits_to_f32(o) - base)
-        # bf16 ulp at |x|: results differ only by summation order
-        ulp = np.abs(base) * 2.0 ** -7 + 1e-30
-        assert np.all(d <= 2 * ulp + 1e-6), f"S={S} moved an output by more than 2 bf16 ulp"
+        bound = 2.0 ** -7 * (2 * np.abs(base) + rms)
+        assert np.all(d <= bound), f"S={S}: max change {d.max():.3g} beyond rounding"
 
 
 def test_page_permutation_is_bit_identical(orc):
