@@ -47,6 +47,16 @@
 namespace pd {
 namespace {
 
+// Shared-memory budget of the stage ring per CTA (bytes; at least 2 stages):
+// 64 KB lets three CTAs share an SM for head_dim <= 128; the head_dim-split
+// kernels (256 / 512) do better with 96 KB and two CTAs.
+#ifndef PD_MMA_RING_BYTES_SMALL_D
+#define PD_MMA_RING_BYTES_SMALL_D (64 * 1024)
+#endif
+#ifndef PD_MMA_RING_BYTES_LARGE_D
+#define PD_MMA_RING_BYTES_LARGE_D (96 * 1024)
+#endif
+
 constexpr int kConsumerWarps = 4;
 constexpr int kMmaThreads = (kConsumerWarps + 1) * 32;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
@@ -262,14 +272,16 @@ struct Cfg {
   static constexpr int kScaleBytes = FMT == PD_KV_NVFP4 ? kKT * (D / 16) : 0;
   static constexpr int kCacheStageBytes = (kDataBytes + kScaleBytes + 1023) / 1024 * 1024;
   static constexpr int kStageBytes = 2 * kCacheStageBytes;
-  static constexpr int kStagesRaw = (96 * 1024) / kStageBytes;
+  static constexpr int kStagesRaw =
+      (kDSplit == 1 ? PD_MMA_RING_BYTES_SMALL_D : PD_MMA_RING_BYTES_LARGE_D) / kStageBytes;
   static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
   static constexpr int kRingBytes = kStages * kStageBytes;
   // cross-warp score sums (head_dim split): 2 buffers x 4 warps x m-tiles x 32 lanes x 4*NT
   static constexpr int kRedBytes = kDSplit == 4 ? 2 * 4 * kMT * 32 * 4 * NT * 4 : 0;
   static constexpr int kMergeBytes = kDSplit == 1 ? 4 * (kDS * 8 * NT + 2 * 8 * NT) * 4 : 0;
   static_assert(kMergeBytes <= kRingBytes, "the end-of-CTA merge reuses the ring");
-  static constexpr int kBarOffset = kRingBytes + kRedBytes;
+  static constexpr int kQMaxBytes = kDSplit == 4 ? 2 * 4 * 8 * 4 : 0;  // [NT][warp][8] floats
+  static constexpr int kBarOffset = kRingBytes + kRedBytes + kQMaxBytes;
   static constexpr int kSmemBytes = kBarOffset + 2 * kStages * 8 + kStages * 4 + 1024;
   // per copy and cache: bytes landed by TMA
   static constexpr uint32_t kCopyBytes =
@@ -282,6 +294,9 @@ __global__ void __launch_bounds__(kMmaThreads)
                        const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
   using C = Cfg<FMT, D, NT, BS>;
   constexpr bool F16 = C::kF16;
+  // let the dependent combine grid be scheduled as this grid drains (it waits
+  // for this grid's completion before reading the workspace)
+  asm volatile("griddepcontrol.launch_dependents;");
   const int g = blockIdx.x;  // kv head
   const int s = blockIdx.y;  // split
   const int b = blockIdx.z;  // sequence
@@ -317,6 +332,7 @@ __global__ void __launch_bounds__(kMmaThreads)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   unsigned char* ring = smem;
   float* red = reinterpret_cast<float*>(smem + C::kRingBytes);
+  float* qmax_s = reinterpret_cast<float*>(smem + C::kRingBytes + C::kRedBytes);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
   uint64_t* empty_bar = full_bar + C::kStages;
   uint32_t* bad_copies = reinterpret_cast<uint32_t*>(empty_bar + C::kStages);
@@ -419,42 +435,53 @@ __global__ void __launch_bounds__(kMmaThreads)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int n = nt * 8 + r;  // q head row of the B fragment
-      float qdown = 1.0f;
-      if constexpr (F16) {
+      if constexpr (!F16) {
+        qmul[nt][0] = qmul[nt][1] = a.scale_log2;
+#pragma unroll
+        for (int ks = 0; ks < C::kKSteps; ++ks) {
+          uint32_t w0 = 0, w1 = 0;
+          if (n < G) {
+            const uint16_t* p = qb + n * D + d0 + ks * 16 + 2 * c;
+            w0 = *reinterpret_cast<const uint32_t*>(p);
+            w1 = *reinterpret_cast<const uint32_t*>(p + 8);
+          }
+          qf[ks][nt][0] = w0;
+          qf[ks][nt][1] = w1;
+        }
+      } else {
+        // this thread's q values (4 consecutive d per k-step), loaded up front
+        uint2 raw[C::kKSteps];
+#pragma unroll
+        for (int ks = 0; ks < C::kKSteps; ++ks)
+          raw[ks] = (n < G) ? *reinterpret_cast<const uint2*>(qb + n * D + d0 + c * (C::kDS / 4) +
+                                                               4 * ks)
+                            : make_uint2(0u, 0u);
         // power-of-two scale putting max |q| of head n in [2^14, 2^15)
         float m = 0.0f;
-        if (n < G)
-          for (int d = c; d < D; d += 4) m = fmaxf(m, fabsf(bf16_to_f32(qb[n * D + d])));
+#pragma unroll
+        for (int ks = 0; ks < C::kKSteps; ++ks)
+          m = fmaxf(fmaxf(m, fmaxf(fabsf(bf16_lo(raw[ks].x)), fabsf(bf16_hi(raw[ks].x)))),
+                    fmaxf(fabsf(bf16_lo(raw[ks].y)), fabsf(bf16_hi(raw[ks].y))));
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-        const int e = ilog2f(m) - 14;
-        qdown = exp2i(-e);
+        if constexpr (C::kDSplit == 4) {  // the other warps hold the rest of head_dim
+          if (c == 0) qmax_s[(nt * 4 + warp) * 8 + r] = m;
+          consumers_sync();
+          m = fmaxf(fmaxf(qmax_s[(nt * 4 + 0) * 8 + r], qmax_s[(nt * 4 + 1) * 8 + r]),
+                    fmaxf(qmax_s[(nt * 4 + 2) * 8 + r], qmax_s[(nt * 4 + 3) * 8 + r]));
+        }
+        const float qdown = exp2i(14 - ilog2f(m));
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const float mj = __shfl_sync(0xFFFFFFFFu, m, (2 * c + j) * 4);
           qmul[nt][j] = a.scale_log2 * (FMT == PD_KV_FP8_E4M3 ? a.k_scale : 1.0f) *
                         exp2i(ilog2f(mj) - 14);
         }
-      } else {
-        qmul[nt][0] = qmul[nt][1] = a.scale_log2;
-      }
 #pragma unroll
-      for (int ks = 0; ks < C::kKSteps; ++ks) {
-        uint32_t w0 = 0, w1 = 0;
-        if (n < G) {
-          if constexpr (!F16) {
-            const uint16_t* p = qb + n * D + d0 + ks * 16 + 2 * c;
-            w0 = *reinterpret_cast<const uint32_t*>(p);
-            w1 = *reinterpret_cast<const uint32_t*>(p + 8);
-          } else {
-            const uint16_t* p = qb + n * D + d0 + c * (C::kDS / 4) + 4 * ks;
-            const uint2 v = *reinterpret_cast<const uint2*>(p);
-            w0 = pack_f16x2(bf16_lo(v.x) * qdown, bf16_hi(v.x) * qdown);
-            w1 = pack_f16x2(bf16_lo(v.y) * qdown, bf16_hi(v.y) * qdown);
-          }
+        for (int ks = 0; ks < C::kKSteps; ++ks) {
+          qf[ks][nt][0] = pack_f16x2(bf16_lo(raw[ks].x) * qdown, bf16_hi(raw[ks].x) * qdown);
+          qf[ks][nt][1] = pack_f16x2(bf16_lo(raw[ks].y) * qdown, bf16_hi(raw[ks].y) * qdown);
         }
-        qf[ks][nt][0] = w0;
-        qf[ks][nt][1] = w1;
       }
     }
   }

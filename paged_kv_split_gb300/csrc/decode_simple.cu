@@ -44,6 +44,8 @@ __device__ __forceinline__ float load_kv(const uint8_t* __restrict__ cache, int6
 
 template <int FMT, int D>
 __global__ void __launch_bounds__(kThreads) partial_simple_kernel(const DecodeArgs a) {
+  // let the dependent combine grid be scheduled as this grid drains
+  asm volatile("griddepcontrol.launch_dependents;");
   constexpr int kPerLane = D / 32;
   constexpr int kAccMax = kMaxGroup * D / kThreads;
   const int g = blockIdx.x;  // kv head
@@ -165,6 +167,9 @@ __global__ void __launch_bounds__(kThreads) partial_simple_kernel(const DecodeAr
 // 4 consecutive output elements.
 template <int D>
 __global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
+  // Launched as a programmatic dependent of the partial kernel: wait until
+  // that grid has completed and its workspace writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int h = blockIdx.x;
   const int b = blockIdx.y;
   const int S = a.num_splits;
@@ -236,16 +241,34 @@ cudaError_t launch_decode_partial(const DecodeArgs& a, int head_dim, int kv_dtyp
   }
 }
 
+template <int D>
+cudaError_t launch_combine_pdl(const CombineArgs& a, cudaStream_t st) {
+  // Programmatic dependent launch: the combine grid may be scheduled while the
+  // partial kernel drains; griddepcontrol.wait inside keeps it correct.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_q_heads, a.num_seqs);
+  cfg.blockDim = dim3(D / 4);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel<D>, a);
+}
+
 cudaError_t launch_decode_combine(const CombineArgs& a, int head_dim, cudaStream_t st) {
   if (a.num_seqs == 0) return cudaSuccess;
-  const dim3 grid(a.num_q_heads, a.num_seqs);
+  cudaError_t e;
   switch (head_dim) {
-    case 64: combine_kernel<64><<<grid, 16, 0, st>>>(a); break;
-    case 128: combine_kernel<128><<<grid, 32, 0, st>>>(a); break;
-    case 256: combine_kernel<256><<<grid, 64, 0, st>>>(a); break;
-    case 512: combine_kernel<512><<<grid, 128, 0, st>>>(a); break;
+    case 64: e = launch_combine_pdl<64>(a, st); break;
+    case 128: e = launch_combine_pdl<128>(a, st); break;
+    case 256: e = launch_combine_pdl<256>(a, st); break;
+    case 512: e = launch_combine_pdl<512>(a, st); break;
     default: return cudaErrorInvalidValue;
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
