@@ -133,9 +133,23 @@ int pd_choose_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_blo
                          int32_t block_size, int32_t sliding_window, int32_t head_dim,
                          int32_t kv_dtype, int device);
 
-/* The same choice with the SM count given (no CUDA call). */
+/* The same choice with the SM count given (no CUDA call): one CTA per
+ * (sequence, kv head, split), S chosen so that the grid is about one wave of
+ * resident CTAs when every sequence is at its maximum length. */
 int pd_plan_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_blocks_per_seq,
-                       int32_t block_size, int32_t sliding_window, int32_t num_sms);
+                       int32_t block_size, int32_t sliding_window, int32_t head_dim,
+                       int32_t kv_dtype, int32_t num_sms);
+
+/* Split count for known sequence lengths (host array seq_lens[num_seqs], as a
+ * serving scheduler holds them): replays the launch in block order onto the
+ * resident CTA slots with a per-CTA start-up cost, adds the partial and
+ * combine traffic, and returns the S with the smallest estimated time.
+ * Host-only, no CUDA call; returns S >= 1 or a negative pd_status. */
+int pd_plan_num_splits_for_lengths(const int32_t* seq_lens, int32_t num_seqs,
+                                   int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t max_blocks_per_seq, int32_t block_size,
+                                   int32_t sliding_window, int32_t head_dim, int32_t kv_dtype,
+                                   int32_t num_sms);
 
 /* One decode step: split-KV partials then the log-sum-exp combine.
  * out[b, h, :] = bf16( sum_j e_j v_j / sum_j e_j ), e_j = exp(s_j - max s),

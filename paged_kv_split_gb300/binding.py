@@ -36,8 +36,11 @@ _lib.pd_decode_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32]
 _lib.pd_decode_workspace_bytes.restype = _sz
 _lib.pd_choose_num_splits.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_int]
 _lib.pd_choose_num_splits.restype = ctypes.c_int
-_lib.pd_plan_num_splits.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
+_lib.pd_plan_num_splits.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]
 _lib.pd_plan_num_splits.restype = ctypes.c_int
+_lib.pd_plan_num_splits_for_lengths.argtypes = [_P, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                                _i32, _i32]
+_lib.pd_plan_num_splits_for_lengths.restype = ctypes.c_int
 _lib.pd_reshape_and_cache.argtypes = [_P, _P, _P, _P, _P, _i32, _i32, _i32, _i32, _i64, _i32,
                                       _f32, _f32, _P]
 _lib.pd_reshape_and_cache.restype = ctypes.c_int
@@ -110,11 +113,25 @@ def pd_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, num_splits) -> in
 
 
 def pd_plan_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, sliding_window,
-                       num_sms) -> int:
+                       head_dim, kv_dtype, num_sms) -> int:
     s = _lib.pd_plan_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size,
-                                sliding_window, num_sms)
+                                sliding_window, head_dim, _dtype_code(kv_dtype), num_sms)
     if s < 1:
         raise PdError("pd_plan_num_splits", -s)
+    return s
+
+
+def pd_plan_num_splits_for_lengths(seq_lens, num_q_heads, num_kv_heads, max_blocks_per_seq,
+                                   block_size, sliding_window, head_dim, kv_dtype, num_sms) -> int:
+    """Split count for host-known sequence lengths (an int sequence or array)."""
+    import numpy as np
+    lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    s = _lib.pd_plan_num_splits_for_lengths(lens.ctypes.data, lens.size, num_q_heads,
+                                            num_kv_heads, max_blocks_per_seq, block_size,
+                                            sliding_window, head_dim, _dtype_code(kv_dtype),
+                                            num_sms)
+    if s < 1:
+        raise PdError("pd_plan_num_splits_for_lengths", -s)
     return s
 
 

@@ -256,7 +256,15 @@ struct Cfg {
   static constexpr int kDSplit = D <= 128 ? 1 : 4;          // warps sharing head_dim
   static constexpr int kDS = D / kDSplit;                   // head_dim slice per warp (64|128)
   static constexpr int kKSteps = kDS / 16;                  // k-steps of S^T, m-tiles of O^T
-  static constexpr int kKT = kDSplit == 1 ? 64 : 16;        // keys per stage
+  // m-tiles of 16 keys each consumer warp takes per stage (head_dim <= 128),
+  // so that a stage carries enough bytes per dependent chain of loads,
+  // conversions, MMAs and the softmax update
+#ifdef PD_MMA_WM_OVERRIDE
+  static constexpr int kWM = PD_MMA_WM_OVERRIDE;
+#else
+  static constexpr int kWM = 1;  // measured best for every form (one 16-key m-tile per warp)
+#endif
+  static constexpr int kKT = kDSplit == 1 ? 64 * kWM : 16;  // keys per stage
   static constexpr int kMT = kKT / 16;                      // 16-key m-tiles per stage
   static constexpr int kBR = kKT < BS ? kKT : BS;           // rows per copy
   static constexpr int kNCopy = kKT / kBR;                  // copies per stage and cache
@@ -383,21 +391,28 @@ __global__ void __launch_bounds__(kMmaThreads)
           }
         }
       }
+      const uint32_t fb = smem_u32(&full_bar[st]);
       if (lane == 0) {
         if (bad) atomicOr(a.flags, PD_DEV_BAD_PAGE);
         bad_copies[st] = bad;
-        const uint32_t fb = smem_u32(&full_bar[st]);
         mbar_arrive_expect_tx(fb, bytes);
-        const uint32_t kst = smem_u32(ring + st * C::kStageBytes);
-        const uint32_t vst = kst + C::kCacheStageBytes;
+      }
+      __syncwarp();
+      // one lane per page issues that page's copies, in parallel
+      {
+        int my_page = -1;
 #pragma unroll
-        for (int j = 0; j < C::kNCopy; ++j) {
-          if (pages[j] < 0) continue;
+        for (int j = 0; j < C::kNCopy; ++j)
+          if (lane == j) my_page = pages[j];
+        if (lane < C::kNCopy && my_page >= 0) {
+          const int j = lane;
+          const uint32_t kst = smem_u32(ring + st * C::kStageBytes);
+          const uint32_t vst = kst + C::kCacheStageBytes;
           const int row0 = (t0 + j * C::kBR) % bs;
           if constexpr (FMT == PD_KV_NVFP4) {
             const int64_t line = static_cast<int64_t>(g) * bs + row0;
-            const uint8_t* kp = a.k_cache + pages[j] * a.page_bytes;
-            const uint8_t* vp = a.v_cache + pages[j] * a.page_bytes;
+            const uint8_t* kp = a.k_cache + my_page * a.page_bytes;
+            const uint8_t* vp = a.v_cache + my_page * a.page_bytes;
             constexpr uint32_t db = C::kBR * (D / 2);
             constexpr uint32_t sb = C::kBR * (D / 16);
             const uint32_t doff = j * db;
@@ -407,7 +422,7 @@ __global__ void __launch_bounds__(kMmaThreads)
             bulk_load(kst + soff, kp + a.data_bytes + line * (D / 16), sb, fb);
             bulk_load(vst + soff, vp + a.data_bytes + line * (D / 16), sb, fb);
           } else {
-            const int z = pages[j] * bs + row0;
+            const int z = my_page * bs + row0;
 #pragma unroll
             for (int ch = 0; ch < C::kDCH; ++ch) {
               const uint32_t off = ch * (C::kKT * C::kCRB) + j * (C::kBR * C::kCRB);
@@ -516,125 +531,247 @@ __global__ void __launch_bounds__(kMmaThreads)
     const uint32_t bad = bad_copies[st];
     const int t0 = t_base + i * C::kKT;
 
-#pragma unroll
-    for (int mtl = 0; mtl < (C::kDSplit == 1 ? 1 : C::kMT); ++mtl) {
-      const int mt = C::kDSplit == 1 ? warp : mtl;  // m-tile within the stage
-      const int key0 = mt * 16;                     // first key of the m-tile in the stage
-
-      // ---------------- S^T = K Q^T over this warp's slice ----------------
-      float sc[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.0f;
-      if constexpr (FMT == PD_KV_BF16) {
-        const int mi = lane >> 3, ri = lane & 7;
-        const int key = key0 + ri + 8 * (mi & 1);
-#pragma unroll
-        for (int ks = 0; ks < C::kKSteps; ++ks) {
-          const int d = d0 + ks * 16 + 8 * (mi >> 1);
-          const uint32_t off = (d / 64) * (C::kKT * 128) + key * 128 + (d % 64) * 2;
-          uint32_t af[4];
-          ldsm_x4(kst + swz128(off), af);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            mma16816<false>(sc[nt], af, qf[ks][nt][0], qf[ks][nt][1]);
-        }
-      } else if constexpr (FMT == PD_KV_FP8_E4M3) {
-        // keys key0+r, key0+r+8: bytes d in [c*DS/4, +DS/4) = kKSteps words
-        uint32_t wa[C::kKSteps], wb[C::kKSteps];
-        const int dbyte = d0 + c * (C::kDS / 4);
-        const uint32_t base = (dbyte / C::kCRB) * (C::kKT * C::kCRB) + (dbyte % C::kCRB);
-#pragma unroll
-        for (int q4 = 0; q4 < C::kKSteps / 4; ++q4) {
-          const uint32_t offa = base + (key0 + r) * C::kCRB + 16 * q4;
-          lds_words<16>(kst + swz<C::kSwizzle>(offa), wa + 4 * q4);
-          lds_words<16>(kst + swz<C::kSwizzle>(offa + 8 * C::kCRB), wb + 4 * q4);
-        }
-#pragma unroll
-        for (int ks = 0; ks < C::kKSteps; ++ks) {
-          uint32_t af[4];
-          af[0] = e4m3x2_f16x2(wa[ks] & 0xFFFFu);
-          af[1] = e4m3x2_f16x2(wb[ks] & 0xFFFFu);
-          af[2] = e4m3x2_f16x2(wa[ks] >> 16);
-          af[3] = e4m3x2_f16x2(wb[ks] >> 16);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            mma16816<true>(sc[nt], af, qf[ks][nt][0], qf[ks][nt][1]);
-        }
-      } else {  // NVFP4
-        constexpr int kB = C::kDS / 8;  // data bytes of this thread's slice per key (8|16)
-        const int dn = d0 + c * (C::kDS / 4);
-        const uint32_t offa = (key0 + r) * (D / 2) + dn / 2;
-        uint32_t wa[kB / 4], wb[kB / 4];
-        lds_words<kB>(kst + offa, wa);
-        lds_words<kB>(kst + offa + 8 * (D / 2), wb);
-        // one E4M3 scale per 16 elements: k-steps 4j..4j+3 use this slice's group j
-        uint32_t sa[C::kKSteps / 4], sbv[C::kKSteps / 4];
-        const uint32_t soa = C::kDataBytes + (key0 + r) * (D / 16) + dn / 16;
-#pragma unroll
-        for (int j = 0; j < C::kKSteps / 4; ++j) {
-          const uint32_t xa = lds_u8(kst + soa + j);
-          const uint32_t xb = lds_u8(kst + soa + 8 * (D / 16) + j);
-          sa[j] = e4m3x2_f16x2(xa | (xa << 8));
-          sbv[j] = e4m3x2_f16x2(xb | (xb << 8));
-        }
-#pragma unroll
-        for (int w = 0; w < kB / 4; ++w) {
-          uint32_t xa[4], xb[4];
-          e2m1x8_f16x2(wa[w], xa);
-          e2m1x8_f16x2(wb[w], xb);
-          // byte 2h of word w -> k-step 2w+h, d +{0,1}; byte 2h+1 -> d +{2,3}
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int ks = 2 * w + h;
-            const int grp = ks / 4;
+      // ---- scores of one 16-key m-tile over this warp's head_dim slice ----
+      auto qk = [&](const int key0, float (&sc)[NT][4]) {
+        if constexpr (FMT == PD_KV_BF16) {
+          const int mi = lane >> 3, ri = lane & 7;
+          const int key = key0 + ri + 8 * (mi & 1);
+  #pragma unroll
+          for (int ks = 0; ks < C::kKSteps; ++ks) {
+            const int d = d0 + ks * 16 + 8 * (mi >> 1);
+            const uint32_t off = (d / 64) * (C::kKT * 128) + key * 128 + (d % 64) * 2;
             uint32_t af[4];
-            af[0] = hmul2_u32(xa[2 * h], sa[grp]);
-            af[1] = hmul2_u32(xb[2 * h], sbv[grp]);
-            af[2] = hmul2_u32(xa[2 * h + 1], sa[grp]);
-            af[3] = hmul2_u32(xb[2 * h + 1], sbv[grp]);
-#pragma unroll
+            ldsm_x4(kst + swz128(off), af);
+  #pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma16816<false>(sc[nt], af, qf[ks][nt][0], qf[ks][nt][1]);
+          }
+        } else if constexpr (FMT == PD_KV_FP8_E4M3) {
+          // keys key0+r, key0+r+8: bytes d in [c*DS/4, +DS/4) = kKSteps words
+          uint32_t wa[C::kKSteps], wb[C::kKSteps];
+          const int dbyte = d0 + c * (C::kDS / 4);
+          const uint32_t base = (dbyte / C::kCRB) * (C::kKT * C::kCRB) + (dbyte % C::kCRB);
+  #pragma unroll
+          for (int q4 = 0; q4 < C::kKSteps / 4; ++q4) {
+            const uint32_t offa = base + (key0 + r) * C::kCRB + 16 * q4;
+            lds_words<16>(kst + swz<C::kSwizzle>(offa), wa + 4 * q4);
+            lds_words<16>(kst + swz<C::kSwizzle>(offa + 8 * C::kCRB), wb + 4 * q4);
+          }
+  #pragma unroll
+          for (int ks = 0; ks < C::kKSteps; ++ks) {
+            uint32_t af[4];
+            af[0] = e4m3x2_f16x2(wa[ks] & 0xFFFFu);
+            af[1] = e4m3x2_f16x2(wb[ks] & 0xFFFFu);
+            af[2] = e4m3x2_f16x2(wa[ks] >> 16);
+            af[3] = e4m3x2_f16x2(wb[ks] >> 16);
+  #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma16816<true>(sc[nt], af, qf[ks][nt][0], qf[ks][nt][1]);
           }
-        }
-      }
-
-      // ---------------- sum the head_dim slices (head_dim 256/512) ----------
-      if constexpr (C::kDSplit == 4) {
-        float* mine = red + ((red_buf * 4 + warp) * C::kMT + mt) * (32 * 4 * NT);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          *reinterpret_cast<float4*>(mine + (nt * 32 + lane) * 4) =
-              make_float4(sc[nt][0], sc[nt][1], sc[nt][2], sc[nt][3]);
-        consumers_sync();
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const float4 u = *reinterpret_cast<const float4*>(
-                red + ((red_buf * 4 + w) * C::kMT + mt) * (32 * 4 * NT) + (nt * 32 + lane) * 4);
-            t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+        } else {  // NVFP4
+          constexpr int kB = C::kDS / 8;  // data bytes of this thread's slice per key (8|16)
+          const int dn = d0 + c * (C::kDS / 4);
+          const uint32_t offa = (key0 + r) * (D / 2) + dn / 2;
+          uint32_t wa[kB / 4], wb[kB / 4];
+          lds_words<kB>(kst + offa, wa);
+          lds_words<kB>(kst + offa + 8 * (D / 2), wb);
+          // one E4M3 scale per 16 elements: k-steps 4j..4j+3 use this slice's group j
+          uint32_t sa[C::kKSteps / 4], sbv[C::kKSteps / 4];
+          const uint32_t soa = C::kDataBytes + (key0 + r) * (D / 16) + dn / 16;
+  #pragma unroll
+          for (int j = 0; j < C::kKSteps / 4; ++j) {
+            const uint32_t xa = lds_u8(kst + soa + j);
+            const uint32_t xb = lds_u8(kst + soa + 8 * (D / 16) + j);
+            sa[j] = e4m3x2_f16x2(xa | (xa << 8));
+            sbv[j] = e4m3x2_f16x2(xb | (xb << 8));
           }
-          sc[nt][0] = t.x; sc[nt][1] = t.y; sc[nt][2] = t.z; sc[nt][3] = t.w;
+  #pragma unroll
+          for (int w = 0; w < kB / 4; ++w) {
+            uint32_t xa[4], xb[4];
+            e2m1x8_f16x2(wa[w], xa);
+            e2m1x8_f16x2(wb[w], xb);
+            // byte 2h of word w -> k-step 2w+h, d +{0,1}; byte 2h+1 -> d +{2,3}
+  #pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int ks = 2 * w + h;
+              const int grp = ks / 4;
+              uint32_t af[4];
+              af[0] = hmul2_u32(xa[2 * h], sa[grp]);
+              af[1] = hmul2_u32(xb[2 * h], sbv[grp]);
+              af[2] = hmul2_u32(xa[2 * h + 1], sa[grp]);
+              af[3] = hmul2_u32(xb[2 * h + 1], sbv[grp]);
+  #pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                mma16816<true>(sc[nt], af, qf[ks][nt][0], qf[ks][nt][1]);
+            }
+          }
         }
-      }
 
-      // ---------------- mask, scale, online softmax ----------------
-      // fragment rows r (c0,c1) and r+8 (c2,c3) are keys key0+r and key0+r+8
+      };
+      // ---- O^T += V^T P^T for one m-tile (masked keys' V halves zeroed) ----
+      auto pv = [&](const int key0, const uint32_t (&pbf)[NT][2], const uint32_t keep_lo,
+                    const uint32_t keep_hi) {
+        if constexpr (FMT == PD_KV_BF16) {
+          const int mi = lane >> 3, ri = lane & 7;
+          const int key = key0 + ri + 8 * (mi >> 1);
+  #pragma unroll
+          for (int md = 0; md < C::kKSteps; ++md) {
+            const int d = d0 + md * 16 + 8 * (mi & 1);
+            const uint32_t off = (d / 64) * (C::kKT * 128) + key * 128 + (d % 64) * 2;
+            uint32_t af[4];
+            ldsm_x4_trans(vst + swz128(off), af);
+            af[0] &= keep_lo;
+            af[1] &= keep_lo;
+            af[2] &= keep_hi;
+            af[3] &= keep_hi;
+  #pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma16816<false>(acc[md][nt], af, pbf[nt][0], pbf[nt][1]);
+          }
+        } else if constexpr (FMT == PD_KV_FP8_E4M3) {
+          // V bytes d in [r*DS/8, (r+1)*DS/8) of keys 2c, 2c+1, 2c+8, 2c+9; byte j is
+          // head_dim row (m-tile j, row r) for j < DS/16 and (j - DS/16, row r+8) above
+          constexpr int kVB = C::kDS / 8;  // 16 or 8
+          const int dbyte = d0 + r * kVB;
+          const uint32_t base = (dbyte / C::kCRB) * (C::kKT * C::kCRB) + (dbyte % C::kCRB);
+          uint32_t v[4][kVB / 4];
+  #pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int key = key0 + 2 * c + (k4 & 1) + 8 * (k4 >> 1);
+            lds_words<kVB>(vst + swz<C::kSwizzle>(base + key * C::kCRB), v[k4]);
+          }
+          // interleave the bytes of the key pairs: PRMT gives {a_j, b_j, a_j+1, b_j+1}
+          uint32_t pr01[kVB / 2], pr23[kVB / 2];
+  #pragma unroll
+          for (int w = 0; w < kVB / 4; ++w) {
+            pr01[2 * w] = __byte_perm(v[0][w], v[1][w], 0x5140);
+            pr01[2 * w + 1] = __byte_perm(v[0][w], v[1][w], 0x7362);
+            pr23[2 * w] = __byte_perm(v[2][w], v[3][w], 0x5140);
+            pr23[2 * w + 1] = __byte_perm(v[2][w], v[3][w], 0x7362);
+          }
+          // byte pair j sits in pr[j / 2], half j % 2
+  #pragma unroll
+          for (int md = 0; md < C::kKSteps; ++md) {
+            const int jl = md, jh = md + C::kKSteps;
+            uint32_t af[4];
+            af[0] = e4m3x2_f16x2(pr01[jl >> 1] >> (16 * (jl & 1))) & keep_lo;
+            af[1] = e4m3x2_f16x2(pr01[jh >> 1] >> (16 * (jh & 1))) & keep_lo;
+            af[2] = e4m3x2_f16x2(pr23[jl >> 1] >> (16 * (jl & 1))) & keep_hi;
+            af[3] = e4m3x2_f16x2(pr23[jh >> 1] >> (16 * (jh & 1))) & keep_hi;
+  #pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma16816<true>(acc[md][nt], af, pbf[nt][0], pbf[nt][1]);
+          }
+        } else {  // NVFP4
+          // V nibbles d in [r*DS/8, (r+1)*DS/8) of keys 2c, 2c+1, 2c+8, 2c+9 (one scale
+          // group per key); nibble j is head_dim row (j, r) below DS/16, else (j - DS/16, r+8)
+          constexpr int kVB = C::kDS / 16;  // data bytes per key (8 or 4)
+          const int dn = d0 + r * (C::kDS / 8);
+          uint32_t v[4][2];
+          uint32_t sv[4];
+  #pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int key = key0 + 2 * c + (k4 & 1) + 8 * (k4 >> 1);
+            v[k4][1] = 0u;
+            lds_words<kVB>(vst + key * (D / 2) + dn / 2, v[k4]);
+            sv[k4] = lds_u8(vst + C::kDataBytes + key * (D / 16) + dn / 16);
+          }
+          const uint32_t s01 = e4m3x2_f16x2(sv[0] | (sv[1] << 8));
+          const uint32_t s23 = e4m3x2_f16x2(sv[2] | (sv[3] << 8));
+          // pair bytes (a_j | b_j << 4): even j from the low nibbles, odd j from the high
+          uint32_t f01[2 * kVB], f23[2 * kVB];  // f16x2 per nibble index j
+  #pragma unroll
+          for (int w = 0; w < kVB / 4; ++w) {
+            const uint32_t e01 = (v[0][w] & 0x0F0F0F0Fu) | ((v[1][w] & 0x0F0F0F0Fu) << 4);
+            const uint32_t o01 = ((v[0][w] >> 4) & 0x0F0F0F0Fu) | (v[1][w] & 0xF0F0F0F0u);
+            const uint32_t e23 = (v[2][w] & 0x0F0F0F0Fu) | ((v[3][w] & 0x0F0F0F0Fu) << 4);
+            const uint32_t o23 = ((v[2][w] >> 4) & 0x0F0F0F0Fu) | (v[3][w] & 0xF0F0F0F0u);
+            uint32_t t[4];
+            e2m1x8_f16x2(e01, t);
+  #pragma unroll
+            for (int k = 0; k < 4; ++k) f01[8 * w + 2 * k] = hmul2_u32(t[k], s01);
+            e2m1x8_f16x2(o01, t);
+  #pragma unroll
+            for (int k = 0; k < 4; ++k) f01[8 * w + 2 * k + 1] = hmul2_u32(t[k], s01);
+            e2m1x8_f16x2(e23, t);
+  #pragma unroll
+            for (int k = 0; k < 4; ++k) f23[8 * w + 2 * k] = hmul2_u32(t[k], s23);
+            e2m1x8_f16x2(o23, t);
+  #pragma unroll
+            for (int k = 0; k < 4; ++k) f23[8 * w + 2 * k + 1] = hmul2_u32(t[k], s23);
+          }
+  #pragma unroll
+          for (int md = 0; md < C::kKSteps; ++md) {
+            uint32_t af[4];
+            af[0] = f01[md] & keep_lo;
+            af[1] = f01[md + C::kKSteps] & keep_lo;
+            af[2] = f23[md] & keep_hi;
+            af[3] = f23[md + C::kKSteps] & keep_hi;
+  #pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma16816<true>(acc[md][nt], af, pbf[nt][0], pbf[nt][1]);
+          }
+        }
+      };
       auto key_ok = [&](int kk) {  // kk: key index within the stage
         const int kabs = t0 + kk;
         return kabs >= t_begin && kabs < t_end && !((bad >> (kk / C::kBR)) & 1u);
       };
-      const bool va = key_ok(key0 + r), vb = key_ok(key0 + r + 8);
-      float p[NT][4];
+      // m-tiles this warp handles in this stage: its own kWM (keys split across
+      // warps) or all of them (head_dim split across warps)
+      constexpr int kU = C::kDSplit == 1 ? C::kWM : C::kMT;
+      auto mt_of = [&](int u) { return C::kDSplit == 1 ? warp * C::kWM + u : u; };
+
+      float sc[kU][NT][4];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) sc[u][nt][0] = sc[u][nt][1] = sc[u][nt][2] = sc[u][nt][3] = 0.0f;
+        qk(mt_of(u) * 16, sc[u]);
+      }
+
+      // ---------------- sum the head_dim slices (head_dim 256/512) ----------
+      if constexpr (C::kDSplit == 4) {
+        float* mine = red + (red_buf * 4 + warp) * (kU * NT * 32 * 4);
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            *reinterpret_cast<float4*>(mine + ((u * NT + nt) * 32 + lane) * 4) =
+                make_float4(sc[u][nt][0], sc[u][nt][1], sc[u][nt][2], sc[u][nt][3]);
+        consumers_sync();
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const float4 v = *reinterpret_cast<const float4*>(
+                  red + (red_buf * 4 + w) * (kU * NT * 32 * 4) + ((u * NT + nt) * 32 + lane) * 4);
+              t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
+            }
+            sc[u][nt][0] = t.x; sc[u][nt][1] = t.y; sc[u][nt][2] = t.z; sc[u][nt][3] = t.w;
+          }
+      }
+
+      // ---------------- mask, scale, one online-softmax update ----------------
+      // fragment rows r (c0,c1) and r+8 (c2,c3) of m-tile u are keys 16*mt + r, +8
+      float p[kU][NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const float x0 = va ? sc[nt][0] * qmul[nt][0] : -INFINITY;
-        const float x1 = va ? sc[nt][1] * qmul[nt][1] : -INFINITY;
-        const float x2 = vb ? sc[nt][2] * qmul[nt][0] : -INFINITY;
-        const float x3 = vb ? sc[nt][3] * qmul[nt][1] : -INFINITY;
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int key0 = mt_of(u) * 16;
+          const bool va = key_ok(key0 + r), vb = key_ok(key0 + r + 8);
+          p[u][nt][0] = va ? sc[u][nt][0] * qmul[nt][0] : -INFINITY;
+          p[u][nt][1] = va ? sc[u][nt][1] * qmul[nt][1] : -INFINITY;
+          p[u][nt][2] = vb ? sc[u][nt][2] * qmul[nt][0] : -INFINITY;
+          p[u][nt][3] = vb ? sc[u][nt][3] * qmul[nt][1] : -INFINITY;
+          mx0 = fmaxf(mx0, fmaxf(p[u][nt][0], p[u][nt][2]));
+          mx1 = fmaxf(mx1, fmaxf(p[u][nt][1], p[u][nt][3]));
+        }
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
           mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, o));
@@ -645,12 +782,18 @@ __global__ void __launch_bounds__(kMmaThreads)
         const float al1 = (mn1 == -INFINITY) ? 1.0f : ex2(m_run[nt][1] - mn1);
         m_run[nt][0] = mn0;
         m_run[nt][1] = mn1;
-        p[nt][0] = (mn0 == -INFINITY) ? 0.0f : ex2(x0 - mn0);
-        p[nt][1] = (mn1 == -INFINITY) ? 0.0f : ex2(x1 - mn1);
-        p[nt][2] = (mn0 == -INFINITY) ? 0.0f : ex2(x2 - mn0);
-        p[nt][3] = (mn1 == -INFINITY) ? 0.0f : ex2(x3 - mn1);
-        l_run[nt][0] = l_run[nt][0] * al0 + p[nt][0] + p[nt][2];
-        l_run[nt][1] = l_run[nt][1] * al1 + p[nt][1] + p[nt][3];
+        float ls0 = 0.0f, ls1 = 0.0f;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          p[u][nt][0] = (mn0 == -INFINITY) ? 0.0f : ex2(p[u][nt][0] - mn0);
+          p[u][nt][1] = (mn1 == -INFINITY) ? 0.0f : ex2(p[u][nt][1] - mn1);
+          p[u][nt][2] = (mn0 == -INFINITY) ? 0.0f : ex2(p[u][nt][2] - mn0);
+          p[u][nt][3] = (mn1 == -INFINITY) ? 0.0f : ex2(p[u][nt][3] - mn1);
+          ls0 += p[u][nt][0] + p[u][nt][2];
+          ls1 += p[u][nt][1] + p[u][nt][3];
+        }
+        l_run[nt][0] = l_run[nt][0] * al0 + ls0;
+        l_run[nt][1] = l_run[nt][1] * al1 + ls1;
 #pragma unroll
         for (int md = 0; md < C::kKSteps; ++md) {
           acc[md][nt][0] *= al0;
@@ -659,133 +802,34 @@ __global__ void __launch_bounds__(kMmaThreads)
           acc[md][nt][3] *= al1;
         }
       }
-      // P^T as B fragments: the 8x8 blocks have keys as rows, q heads as columns
-      uint32_t pbf[NT][2];
+
+      // ---------------- O^T += V^T P^T, m-tile by m-tile ----------------
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const uint32_t top =
-            F16 ? pack_f16x2(p[nt][0], p[nt][1]) : pack_bf16x2(p[nt][0], p[nt][1]);
-        const uint32_t bot =
-            F16 ? pack_f16x2(p[nt][2], p[nt][3]) : pack_bf16x2(p[nt][2], p[nt][3]);
-        pbf[nt][0] = movmatrix_trans(top);
-        pbf[nt][1] = movmatrix_trans(bot);
+      for (int u = 0; u < kU; ++u) {
+        const int key0 = mt_of(u) * 16;
+        // P^T as B fragments: the 8x8 blocks have keys as rows, q heads as columns
+        uint32_t pbf[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint32_t top = F16 ? pack_f16x2(p[u][nt][0], p[u][nt][1])
+                                   : pack_bf16x2(p[u][nt][0], p[u][nt][1]);
+          const uint32_t bot = F16 ? pack_f16x2(p[u][nt][2], p[u][nt][3])
+                                   : pack_bf16x2(p[u][nt][2], p[u][nt][3]);
+          pbf[nt][0] = movmatrix_trans(top);
+          pbf[nt][1] = movmatrix_trans(bot);
+        }
+        uint32_t keep_lo = 0xFFFFFFFFu, keep_hi = 0xFFFFFFFFu;
+        const bool ragged = (t0 + key0 < t_begin) || (t0 + key0 + 16 > t_end) ||
+                            ((bad >> (key0 / C::kBR)) & 1u);
+        if (ragged) {
+          keep_lo = (key_ok(key0 + 2 * c) ? 0x0000FFFFu : 0u) |
+                    (key_ok(key0 + 2 * c + 1) ? 0xFFFF0000u : 0u);
+          keep_hi = (key_ok(key0 + 2 * c + 8) ? 0x0000FFFFu : 0u) |
+                    (key_ok(key0 + 2 * c + 9) ? 0xFFFF0000u : 0u);
+        }
+        pv(key0, pbf, keep_lo, keep_hi);
       }
 
-      // ---------------- O^T += V^T P^T ----------------
-      // A-fragment columns are keys 2c, 2c+1 (low / high halves) and 2c+8, 2c+9;
-      // masked keys have P = 0, and their V halves are zeroed so that any NaN
-      // or Inf bytes in unused cache rows cannot leak in as 0 * NaN.
-      uint32_t keep_lo = 0xFFFFFFFFu, keep_hi = 0xFFFFFFFFu;
-      const bool ragged = (t0 + key0 < t_begin) || (t0 + key0 + 16 > t_end) ||
-                          ((bad >> (key0 / C::kBR)) & 1u);
-      if (ragged) {
-        keep_lo = (key_ok(key0 + 2 * c) ? 0x0000FFFFu : 0u) |
-                  (key_ok(key0 + 2 * c + 1) ? 0xFFFF0000u : 0u);
-        keep_hi = (key_ok(key0 + 2 * c + 8) ? 0x0000FFFFu : 0u) |
-                  (key_ok(key0 + 2 * c + 9) ? 0xFFFF0000u : 0u);
-      }
-      if constexpr (FMT == PD_KV_BF16) {
-        const int mi = lane >> 3, ri = lane & 7;
-        const int key = key0 + ri + 8 * (mi >> 1);
-#pragma unroll
-        for (int md = 0; md < C::kKSteps; ++md) {
-          const int d = d0 + md * 16 + 8 * (mi & 1);
-          const uint32_t off = (d / 64) * (C::kKT * 128) + key * 128 + (d % 64) * 2;
-          uint32_t af[4];
-          ldsm_x4_trans(vst + swz128(off), af);
-          af[0] &= keep_lo;
-          af[1] &= keep_lo;
-          af[2] &= keep_hi;
-          af[3] &= keep_hi;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            mma16816<false>(acc[md][nt], af, pbf[nt][0], pbf[nt][1]);
-        }
-      } else if constexpr (FMT == PD_KV_FP8_E4M3) {
-        // V bytes d in [r*DS/8, (r+1)*DS/8) of keys 2c, 2c+1, 2c+8, 2c+9; byte j is
-        // head_dim row (m-tile j, row r) for j < DS/16 and (j - DS/16, row r+8) above
-        constexpr int kVB = C::kDS / 8;  // 16 or 8
-        const int dbyte = d0 + r * kVB;
-        const uint32_t base = (dbyte / C::kCRB) * (C::kKT * C::kCRB) + (dbyte % C::kCRB);
-        uint32_t v[4][kVB / 4];
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const int key = key0 + 2 * c + (k4 & 1) + 8 * (k4 >> 1);
-          lds_words<kVB>(vst + swz<C::kSwizzle>(base + key * C::kCRB), v[k4]);
-        }
-        // interleave the bytes of the key pairs: PRMT gives {a_j, b_j, a_j+1, b_j+1}
-        uint32_t pr01[kVB / 2], pr23[kVB / 2];
-#pragma unroll
-        for (int w = 0; w < kVB / 4; ++w) {
-          pr01[2 * w] = __byte_perm(v[0][w], v[1][w], 0x5140);
-          pr01[2 * w + 1] = __byte_perm(v[0][w], v[1][w], 0x7362);
-          pr23[2 * w] = __byte_perm(v[2][w], v[3][w], 0x5140);
-          pr23[2 * w + 1] = __byte_perm(v[2][w], v[3][w], 0x7362);
-        }
-        // byte pair j sits in pr[j / 2], half j % 2
-#pragma unroll
-        for (int md = 0; md < C::kKSteps; ++md) {
-          const int jl = md, jh = md + C::kKSteps;
-          uint32_t af[4];
-          af[0] = e4m3x2_f16x2(pr01[jl >> 1] >> (16 * (jl & 1))) & keep_lo;
-          af[1] = e4m3x2_f16x2(pr01[jh >> 1] >> (16 * (jh & 1))) & keep_lo;
-          af[2] = e4m3x2_f16x2(pr23[jl >> 1] >> (16 * (jl & 1))) & keep_hi;
-          af[3] = e4m3x2_f16x2(pr23[jh >> 1] >> (16 * (jh & 1))) & keep_hi;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            mma16816<true>(acc[md][nt], af, pbf[nt][0], pbf[nt][1]);
-        }
-      } else {  // NVFP4
-        // V nibbles d in [r*DS/8, (r+1)*DS/8) of keys 2c, 2c+1, 2c+8, 2c+9 (one scale
-        // group per key); nibble j is head_dim row (j, r) below DS/16, else (j - DS/16, r+8)
-        constexpr int kVB = C::kDS / 16;  // data bytes per key (8 or 4)
-        const int dn = d0 + r * (C::kDS / 8);
-        uint32_t v[4][2];
-        uint32_t sv[4];
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const int key = key0 + 2 * c + (k4 & 1) + 8 * (k4 >> 1);
-          v[k4][1] = 0u;
-          lds_words<kVB>(vst + key * (D / 2) + dn / 2, v[k4]);
-          sv[k4] = lds_u8(vst + C::kDataBytes + key * (D / 16) + dn / 16);
-        }
-        const uint32_t s01 = e4m3x2_f16x2(sv[0] | (sv[1] << 8));
-        const uint32_t s23 = e4m3x2_f16x2(sv[2] | (sv[3] << 8));
-        // pair bytes (a_j | b_j << 4): even j from the low nibbles, odd j from the high
-        uint32_t f01[2 * kVB], f23[2 * kVB];  // f16x2 per nibble index j
-#pragma unroll
-        for (int w = 0; w < kVB / 4; ++w) {
-          const uint32_t e01 = (v[0][w] & 0x0F0F0F0Fu) | ((v[1][w] & 0x0F0F0F0Fu) << 4);
-          const uint32_t o01 = ((v[0][w] >> 4) & 0x0F0F0F0Fu) | (v[1][w] & 0xF0F0F0F0u);
-          const uint32_t e23 = (v[2][w] & 0x0F0F0F0Fu) | ((v[3][w] & 0x0F0F0F0Fu) << 4);
-          const uint32_t o23 = ((v[2][w] >> 4) & 0x0F0F0F0Fu) | (v[3][w] & 0xF0F0F0F0u);
-          uint32_t t[4];
-          e2m1x8_f16x2(e01, t);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) f01[8 * w + 2 * k] = hmul2_u32(t[k], s01);
-          e2m1x8_f16x2(o01, t);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) f01[8 * w + 2 * k + 1] = hmul2_u32(t[k], s01);
-          e2m1x8_f16x2(e23, t);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) f23[8 * w + 2 * k] = hmul2_u32(t[k], s23);
-          e2m1x8_f16x2(o23, t);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) f23[8 * w + 2 * k + 1] = hmul2_u32(t[k], s23);
-        }
-#pragma unroll
-        for (int md = 0; md < C::kKSteps; ++md) {
-          uint32_t af[4];
-          af[0] = f01[md] & keep_lo;
-          af[1] = f01[md + C::kKSteps] & keep_lo;
-          af[2] = f23[md] & keep_hi;
-          af[3] = f23[md + C::kKSteps] & keep_hi;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            mma16816<true>(acc[md][nt], af, pbf[nt][0], pbf[nt][1]);
-        }
-      }
-    }  // m-tiles of the stage
     if constexpr (C::kDSplit == 4) red_buf ^= 1;
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
@@ -963,6 +1007,23 @@ cudaError_t launch_mma_fmt(const DecodeArgs& a, int D, cudaStream_t st) {
 }
 
 }  // namespace
+
+int mma_ctas_per_sm_estimate(int kv_dtype, int head_dim) {
+  auto per_sm = [](int smem) { return (227 * 1024) / (smem + 1024); };
+  int smem;
+  if (kv_dtype == PD_KV_BF16) {
+    smem = head_dim <= 128 ? Cfg<PD_KV_BF16, 128, 1, 16>::kSmemBytes
+                           : Cfg<PD_KV_BF16, 512, 1, 16>::kSmemBytes;
+  } else if (kv_dtype == PD_KV_FP8_E4M3) {
+    smem = head_dim <= 128 ? Cfg<PD_KV_FP8_E4M3, 128, 1, 16>::kSmemBytes
+                           : Cfg<PD_KV_FP8_E4M3, 512, 1, 16>::kSmemBytes;
+  } else {
+    smem = head_dim <= 128 ? Cfg<PD_KV_NVFP4, 128, 1, 16>::kSmemBytes
+                           : Cfg<PD_KV_NVFP4, 512, 1, 16>::kSmemBytes;
+  }
+  const int n = per_sm(smem);
+  return n < 1 ? 1 : (n > 4 ? 4 : n);
+}
 
 cudaError_t launch_decode_partial_mma(const DecodeArgs& a, int head_dim, int kv_dtype,
                                       cudaStream_t st) {

@@ -5,7 +5,10 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
+#include <functional>
 #include <mutex>
+#include <vector>
 
 #include "pd_common.cuh"
 
@@ -124,20 +127,84 @@ CombineArgs make_combine_args(int B, int Hq, int D, int bs, int mbs, int S, int 
   return c;
 }
 
-int plan_splits(int B, int Hkv, int mbs, int bs, int W, int num_sms) {
-  // Work units without splitting: one CTA per (sequence, kv head). Aim for
-  // a few resident CTAs per SM, but keep at least ~4 pages of 16 (64 keys)
-  // per split so the partial write stays small against the KV read.
+// Bytes of K + V one (page, kv head) holds.
+double page_head_bytes(int bs, int D, int kv_dtype) {
+  const double elem = kv_dtype == PD_KV_BF16 ? 2.0 : (kv_dtype == PD_KV_FP8_E4M3 ? 1.0 : 0.5625);
+  return static_cast<double>(bs) * 2.0 * D * elem;
+}
+
+// Shape-only split count: one CTA per (sequence, kv head, split) with about
+// one wave of resident CTAs when every sequence is at its maximum length.
+int plan_splits(int B, int Hkv, int mbs, int bs, int W, int num_sms, int ctas_per_sm) {
   const int span = page_span_max(mbs, bs, W);
   const int64_t units = static_cast<int64_t>(B > 0 ? B : 1) * (Hkv > 0 ? Hkv : 1);
-  const int64_t target = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 4;
-  int64_t S = (target + units - 1) / units;
-  const int64_t min_pages = (bs >= 32) ? 2 : 4;
-  const int64_t cap = (span + min_pages - 1) / min_pages;
-  if (S > cap) S = cap;
+  const int64_t slots = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * ctas_per_sm;
+  int64_t S = (slots + units / 2) / units;
+  if (S > span) S = span;
   if (S < 1) S = 1;
   if (S > kMaxSplits) S = kMaxSplits;
   return static_cast<int>(S);
+}
+
+// Length-aware split count. For each candidate S it replays the launch in
+// block order (kv head fastest, then split, then sequence) onto `slots`
+// equal-bandwidth CTA slots, each CTA costing a fixed start-up equivalent of
+// kCtaOverheadBytes plus its pages' bytes, and adds the partial-write and
+// combine traffic of the splits that hold keys; the smallest estimated
+// makespan wins (ties: fewer splits).
+constexpr double kCtaOverheadBytes = 40.0 * 1024.0;
+int plan_splits_lengths(const int32_t* lens, int B, int Hkv, int Hq, int mbs, int bs, int W,
+                        int D, int kv_dtype, int num_sms, int ctas_per_sm) {
+  const int span = page_span_max(mbs, bs, W);
+  const int64_t slots = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * ctas_per_sm;
+  const double phb = page_head_bytes(bs, D, kv_dtype);
+  std::vector<int> P(B);
+  const int cap = mbs * bs;
+  for (int b = 0; b < B; ++b) {
+    const int L = lens[b] < 0 ? 0 : (lens[b] > cap ? cap : lens[b]);
+    P[b] = num_key_pages(L, W, bs);
+  }
+  int best_S = 1;
+  double best_t = 1e300;
+  std::vector<double> heap;
+  const int max_S = span < kMaxSplits ? span : kMaxSplits;
+  // candidates: 1..32, a geometric ladder above, and the split counts that
+  // fill one to four waves of resident CTAs exactly
+  std::vector<int> cand;
+  for (int S = 1; S <= max_S; S = (S < 32 ? S + 1 : S + S / 8)) cand.push_back(S);
+  const int64_t units = static_cast<int64_t>(B) * Hkv;
+  for (int k = 1; k <= 4; ++k) {
+    const int64_t w = k * slots / (units > 0 ? units : 1);
+    for (int64_t S = w - 1; S <= w + 1; ++S)
+      if (S >= 1 && S <= max_S) cand.push_back(static_cast<int>(S));
+  }
+  std::sort(cand.begin(), cand.end());
+  cand.erase(std::unique(cand.begin(), cand.end()), cand.end());
+  for (const int S : cand) {
+    const int chunk = chunk_pages(span, S);
+    heap.assign(static_cast<size_t>(slots), 0.0);  // min-heap of slot free times
+    double partial_bytes = 0.0;
+    for (int b = 0; b < B; ++b) {
+      const int n = (P[b] + chunk - 1) / chunk;
+      for (int sp = 0; sp < n; ++sp) {
+        const int pages = (sp == n - 1) ? P[b] - sp * chunk : chunk;
+        const double cost = kCtaOverheadBytes + pages * phb;
+        for (int g = 0; g < Hkv; ++g) {
+          std::pop_heap(heap.begin(), heap.end(), std::greater<double>());
+          heap.back() += cost;
+          std::push_heap(heap.begin(), heap.end(), std::greater<double>());
+        }
+      }
+      if (n > 1) partial_bytes += 2.0 * n * static_cast<double>(Hq / Hkv) * Hkv * (D + 2) * 4.0;
+    }
+    const double span_t = *std::max_element(heap.begin(), heap.end());
+    const double t = span_t + partial_bytes / static_cast<double>(slots);
+    if (t < best_t * (1.0 - 1e-9)) {
+      best_t = t;
+      best_S = S;
+    }
+  }
+  return best_S;
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? PD_OK : PD_ERR_CUDA; }
@@ -191,24 +258,39 @@ size_t pd_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t 
 }
 
 int pd_plan_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_blocks_per_seq,
-                       int32_t block_size, int32_t sliding_window, int32_t num_sms) {
+                       int32_t block_size, int32_t sliding_window, int32_t head_dim,
+                       int32_t kv_dtype, int32_t num_sms) {
   if (num_seqs < 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 ||
-      sliding_window < 0 || num_sms <= 0)
+      sliding_window < 0 || num_sms <= 0 || !head_dim_ok(head_dim) || !dtype_ok(kv_dtype))
     return -PD_ERR_INVALID_ARG;
   return plan_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, sliding_window,
-                     num_sms);
+                     num_sms, mma_ctas_per_sm_estimate(kv_dtype, head_dim));
+}
+
+int pd_plan_num_splits_for_lengths(const int32_t* seq_lens, int32_t num_seqs,
+                                   int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t max_blocks_per_seq, int32_t block_size,
+                                   int32_t sliding_window, int32_t head_dim, int32_t kv_dtype,
+                                   int32_t num_sms) {
+  if (num_seqs < 0 || (num_seqs > 0 && seq_lens == nullptr) || num_kv_heads <= 0 ||
+      num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 || max_blocks_per_seq <= 0 ||
+      block_size <= 0 || sliding_window < 0 || num_sms <= 0 || !head_dim_ok(head_dim) ||
+      !dtype_ok(kv_dtype))
+    return -PD_ERR_INVALID_ARG;
+  if (num_seqs == 0) return 1;
+  return plan_splits_lengths(seq_lens, num_seqs, num_kv_heads, num_q_heads, max_blocks_per_seq,
+                             block_size, sliding_window, head_dim, kv_dtype, num_sms,
+                             mma_ctas_per_sm_estimate(kv_dtype, head_dim));
 }
 
 int pd_choose_num_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_blocks_per_seq,
                          int32_t block_size, int32_t sliding_window, int32_t head_dim,
                          int32_t kv_dtype, int device) {
-  (void)head_dim;
-  (void)kv_dtype;
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
     return -PD_ERR_CUDA;
   return pd_plan_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size,
-                            sliding_window, sms);
+                            sliding_window, head_dim, kv_dtype, sms);
 }
 
 int pd_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
@@ -299,8 +381,9 @@ int pd_decode(const void* q, const void* k_cache, const void* v_cache, const int
     if (current_device(&dev) != cudaSuccess) return PD_ERR_CUDA;
     if (num_kv_heads <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 || sliding_window < 0)
       return PD_ERR_INVALID_ARG;
+    if (!head_dim_ok(head_dim) || !dtype_ok(kv_dtype)) return PD_ERR_UNSUPPORTED;
     S = plan_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, sliding_window,
-                    dev->num_sms);
+                    dev->num_sms, mma_ctas_per_sm_estimate(kv_dtype, head_dim));
   }
   int rc = pd_decode_partial(q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_q_heads,
                              num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,

@@ -184,5 +184,8 @@ cudaError_t launch_decode_partial(const DecodeArgs& a, int head_dim, int kv_dtyp
                                   cudaStream_t st);
 cudaError_t launch_decode_partial_mma(const DecodeArgs& a, int head_dim, int kv_dtype,
                                       cudaStream_t st);
+// Resident CTAs per SM of the tensor-core partial kernel, from its shared
+// memory per CTA (host-only estimate; no CUDA call).
+int mma_ctas_per_sm_estimate(int kv_dtype, int head_dim);
 cudaError_t launch_decode_combine(const CombineArgs& a, int head_dim, cudaStream_t st);
 }  // namespace pd

@@ -63,15 +63,38 @@ def test_cache_and_workspace_sizes(pdlib):
 
 def test_split_planner(pdlib):
     _, L = pdlib
-    L.pd_plan_num_splits.argtypes = [ctypes.c_int32] * 6
-    # few work units -> more splits, bounded by the pages available
-    s_b1 = L.pd_plan_num_splits(1, 8, 1024, 32, 0, 152)
-    s_b64 = L.pd_plan_num_splits(64, 8, 1024, 16, 0, 152)
-    assert s_b1 > s_b64 >= 1
-    assert L.pd_plan_num_splits(1, 1, 1, 16, 0, 152) == 1
-    # a window bounds the pages any split can see
-    assert L.pd_plan_num_splits(1, 4, 1024, 16, 64, 152) <= 2
-    assert L.pd_plan_num_splits(1, 8, 10, 16, 0, 0) < 0
+    L.pd_plan_num_splits.argtypes = [ctypes.c_int32] * 8
+    plan = L.pd_plan_num_splits
+    # (num_seqs, kv heads, max pages, block size, window, head_dim, dtype, SMs):
+    # about one wave of resident CTAs at the maximum length
+    one = plan(4, 8, 1024, 32, 0, 128, 0, 152)
+    assert 8 <= one <= 32
+    assert plan(1, 8, 1024, 32, 0, 128, 0, 152) > one          # fewer units, more splits
+    assert plan(64, 8, 1024, 32, 0, 128, 0, 152) == 1          # enough units already
+    assert plan(1, 1, 1, 16, 0, 128, 0, 152) == 1               # one page, one split
+    assert plan(1, 4, 1024, 16, 64, 128, 0, 152) <= 5           # a window bounds the pages
+    assert plan(1, 8, 10, 16, 0, 128, 0, 0) < 0
+    assert plan(1, 8, 10, 16, 0, 128, 7, 152) < 0
+
+
+def test_split_planner_for_lengths(pdlib):
+    import numpy as np
+    _, L = pdlib
+    f = L.pd_plan_num_splits_for_lengths
+    f.argtypes = [ctypes.c_void_p] + [ctypes.c_int32] * 9
+    lens = np.full(4, 32768, np.int32)
+    S = f(lens.ctypes.data, 4, 32, 8, 1024, 32, 0, 128, 0, 152)
+    # uniform long sequences: fill one wave of CTAs without a second, partial one
+    assert S * 4 * 8 <= 152 * 4 and S >= 8
+    # one long sequence among short ones is cut so that its pieces are no
+    # longer than about a wave's share of the whole batch's pages
+    mixed = np.array([32768] + [512] * 31, np.int32)
+    s_mixed = f(mixed.ctypes.data, 32, 32, 8, 1024, 32, 0, 128, 0, 152)
+    chunk = -(-1024 // s_mixed)
+    total_pages = (1024 + 31 * 16) * 8
+    assert chunk * 8 <= 2 * total_pages / (152 * 3) * 8 + 16
+    assert f(lens.ctypes.data, 4, 30, 8, 1024, 32, 0, 128, 0, 152) < 0   # 30 % 8 != 0
+    assert f(None, 0, 32, 8, 1024, 32, 0, 128, 0, 152) == 1
 
 
 def test_status_strings(pdlib):

@@ -78,6 +78,17 @@ def test_small_parity(orc, kv_dtype, spec):
     run_parity(orc, case, kv_dtype, [1, 3, 0])
 
 
+def test_many_sequences_unscanned_tickets(orc):
+    """More sequences than the persistent kernel scans in shared memory: its
+    tickets then run over every (sequence, split, kv head), empty ones skipped."""
+    lens = inputs.uniform_int(77, 1100, 1, 60)
+    lens[::97] = 0
+    case = inputs.make_case("many", lens, 4, 2, 64, 16, seed=12, extra_blocks=1)
+    case.block_tables[case.block_tables < 0] = 0
+    for kv_dtype in (0, 2):
+        run_parity(orc, case, kv_dtype, [1, 3])
+
+
 def test_split_independence(orc):
     case = inputs.make_case("splits", [2000, 777, 64], 32, 8, 128, 16, seed=5)
     outs, _ = run_parity(orc, case, 0, [1, 2, 4, 16, 64])
