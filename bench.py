@@ -1,9 +1,9 @@
 """Decode benchmark: paged split-KV decode attention on GB300.
 
-One step = one pd_decode (split-KV partial kernel + combine kernel) over the
+One step = one pd_decode (split-KV partial kernel + log-sum-exp combine) over the
 whole batch of the Llama-3-8B-shaped workload (32 sequences, 32 q / 8 kv
 heads, head_dim 128, block_size 16, lengths uniform in [1024, 4096], BF16
-cache, pages shuffled across the pool, splits chosen automatically), inputs
+cache, pages shuffled across the pool, splits from the length-aware planner), inputs
 resident in HBM. Reported value: KV-read GB/s = algorithmic bytes / step time
 (us/step alongside); e2e: the same through the C ABI from pinned host inputs.
 
@@ -270,8 +270,12 @@ def run_pd(args, rank, world, local):
     out = torch.empty_like(q)
     B, hq, D = case.q.shape
     mbs = case.max_blocks_per_seq
-    S = args.splits or pd.pd_choose_num_splits(B, case.num_kv_heads, mbs, case.block_size,
-                                               case.sliding_window, D, kv_dtype, dev.index)
+    # the host holds the batch's lengths (as a serving scheduler does), so the
+    # split count comes from the length-aware planner unless one is given
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    S = args.splits or pd.pd_plan_num_splits_for_lengths(
+        case.seq_lens, hq, case.num_kv_heads, mbs, case.block_size, case.sliding_window, D,
+        kv_dtype, sms)
     ws = torch.empty(pd.pd_decode_workspace_bytes(B, hq, D, S), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     common = dict(num_kv_heads=case.num_kv_heads, block_size=case.block_size,
@@ -279,6 +283,8 @@ def run_pd(args, rank, world, local):
                   sliding_window=case.sliding_window, kv_dtype=kv_dtype, k_scale=ks, v_scale=vs)
 
     def step(i, ev=None):
+        # one decode step = the two halves of pd_decode, with events around the
+        # split-KV partial kernel (the roofline's kernel)
         kc, vc = caches[i % replicas]
         if ev is not None:
             ev[0].record(stream)
@@ -386,6 +392,7 @@ def run_pd(args, rank, world, local):
                        "num_kv_heads": case.num_kv_heads, "head_dim": D,
                        "block_size": case.block_size, "kv_dtype": DTYPE_NAME[kv_dtype],
                        "sliding_window": case.sliding_window, "num_splits": S,
+                       "split_planner": "given" if args.splits else "seq_lens",
                        "keys_per_step": ab["keys"], "algorithmic_bytes_per_step": int(ab["total"]),
                        "workspace_bytes_per_step": int(2 * B * hq * S * (D + 2) * 4),
                        "l2": f"inputs larger than L2: {replicas} cache replicas of "

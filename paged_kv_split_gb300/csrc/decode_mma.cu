@@ -327,7 +327,15 @@ __global__ void __launch_bounds__(kMmaThreads)
   }
   const int lo = window_lo(L, a.sliding_window);
   const int P = num_key_pages(L, a.sliding_window, bs);
-  if (s * a.chunk >= P) return;  // no key of this sequence falls in this split
+  if (s * a.chunk >= P) {  // no key of this sequence falls in this split
+    if (a.direct && P == 0 && s == 0) {  // an empty sequence: zero output rows
+      uint16_t* o = a.out + (static_cast<int64_t>(b) * a.num_q_heads + g * G) * D;
+      for (int e = tid; e < G * D; e += blockDim.x) o[e] = 0;
+    }
+    return;
+  }
+  const int n_act = (P + a.chunk - 1) / a.chunk;  // splits of this sequence that hold keys
+  const bool direct = a.direct && n_act == 1;      // this split alone: write the output
   const int first_page = lo / bs + s * a.chunk;
   const int last_page = min(lo / bs + P, first_page + a.chunk);  // exclusive
   const int t_base = first_page * bs;                             // tile origin (page aligned)
@@ -852,26 +860,37 @@ __global__ void __launch_bounds__(kMmaThreads)
   };
   const int64_t row0 = (static_cast<int64_t>(b) * a.num_q_heads + g * G) * a.num_splits + s;
 
+  const int64_t orow0 = (static_cast<int64_t>(b) * a.num_q_heads + g * G) * D;  // out row of head 0
   if constexpr (C::kDSplit == 4) {
-    if (failed) return;
     // every warp holds the same (m, l) and its own head_dim slice of O
+    if (!failed) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int h = nt * 8 + 2 * c + j;
-        if (h >= G) continue;
-        const float inv = vmul / fmaxf(l_run[nt][j], 1e-20f);
-        float* o = a.ws_o + (row0 + static_cast<int64_t>(h) * a.num_splits) * D;
+        for (int j = 0; j < 2; ++j) {
+          const int h = nt * 8 + 2 * c + j;
+          if (h >= G) continue;
+          const float inv = vmul / fmaxf(l_run[nt][j], 1e-20f);
+          if (direct) {
+            uint16_t* o = a.out + orow0 + static_cast<int64_t>(h) * D;
 #pragma unroll
-        for (int md = 0; md < C::kKSteps; ++md) {
-          o[drow(md, 0)] = acc[md][nt][j] * inv;
-          o[drow(md, 1)] = acc[md][nt][2 + j] * inv;
+            for (int md = 0; md < C::kKSteps; ++md) {
+              o[drow(md, 0)] = f32_to_bf16(acc[md][nt][j] * inv);
+              o[drow(md, 1)] = f32_to_bf16(acc[md][nt][2 + j] * inv);
+            }
+            continue;
+          }
+          float* o = a.ws_o + (row0 + static_cast<int64_t>(h) * a.num_splits) * D;
+#pragma unroll
+          for (int md = 0; md < C::kKSteps; ++md) {
+            o[drow(md, 0)] = acc[md][nt][j] * inv;
+            o[drow(md, 1)] = acc[md][nt][2 + j] * inv;
+          }
+          if (warp == 0 && r == 0)
+            a.ws_ml[row0 + static_cast<int64_t>(h) * a.num_splits] =
+                make_float2(m_run[nt][j], l_run[nt][j]);
         }
-        if (warp == 0 && r == 0)
-          a.ws_ml[row0 + static_cast<int64_t>(h) * a.num_splits] =
-              make_float2(m_run[nt][j], l_run[nt][j]);
-      }
+    }
   } else {
     // head_dim <= 128: merge the four warps' (m, l, O) through shared memory
     consumers_sync();  // every warp is done with the ring
@@ -895,23 +914,28 @@ __global__ void __launch_bounds__(kMmaThreads)
         }
       }
     consumers_sync();
-    if (failed) return;
-    for (int e = tid; e < G * D; e += kConsumerWarps * 32) {
-      const int h = e / D, d = e % D;
-      float M = -INFINITY;
+    if (!failed) {
+      for (int e = tid; e < G * D; e += kConsumerWarps * 32) {
+        const int h = e / D, d = e % D;
+        float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < 4; ++w) M = fmaxf(M, mrec[w * kHW + h]);
-      float lsum = 0.0f, o = 0.0f;
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, mrec[w * kHW + h]);
+        float lsum = 0.0f, o = 0.0f;
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float mw = mrec[w * kHW + h];
-        const float f = (mw == -INFINITY) ? 0.0f : ex2(mw - M);
-        lsum += lrec[w * kHW + h] * f;
-        o += orec[(w * D + d) * kHW + h] * f;
+        for (int w = 0; w < 4; ++w) {
+          const float mw = mrec[w * kHW + h];
+          const float f = (mw == -INFINITY) ? 0.0f : ex2(mw - M);
+          lsum += lrec[w * kHW + h] * f;
+          o += orec[(w * D + d) * kHW + h] * f;
+        }
+        if (direct) {
+          a.out[orow0 + e] = f32_to_bf16(o * vmul / fmaxf(lsum, 1e-20f));
+          continue;
+        }
+        a.ws_o[(row0 + static_cast<int64_t>(h) * a.num_splits) * D + d] =
+            o * vmul / fmaxf(lsum, 1e-20f);
+        if (d == 0) a.ws_ml[row0 + static_cast<int64_t>(h) * a.num_splits] = make_float2(M, lsum);
       }
-      a.ws_o[(row0 + static_cast<int64_t>(h) * a.num_splits) * D + d] =
-          o * vmul / fmaxf(lsum, 1e-20f);
-      if (d == 0) a.ws_ml[row0 + static_cast<int64_t>(h) * a.num_splits] = make_float2(M, lsum);
     }
   }
 }

@@ -164,12 +164,15 @@ __global__ void __launch_bounds__(kThreads) partial_simple_kernel(const DecodeAr
 }
 
 // Combine: one CTA of D/4 threads per (q head, sequence); each thread owns
-// 4 consecutive output elements.
+// 4 consecutive output elements. The split weights w_s = l_s 2^(m_s - M)
+// are computed once, split-parallel across lanes, into shared memory; the
+// weighted sum over the splits then issues its loads four splits at a time.
 template <int D>
 __global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
   // Launched as a programmatic dependent of the partial kernel: wait until
   // that grid has completed and its workspace writes are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int kThreads = D / 4;
   const int h = blockIdx.x;
   const int b = blockIdx.y;
   const int S = a.num_splits;
@@ -178,21 +181,66 @@ __global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
   L = L < 0 ? 0 : (L > cap ? cap : L);
   const int P = num_key_pages(L, a.sliding_window, a.block_size);
   const int n = min((P + a.chunk - 1) / a.chunk, S);  // splits holding keys
+  if (a.skip_direct && n <= 1) return;  // the partial kernel wrote this row
   const int64_t row0 = (static_cast<int64_t>(b) * a.num_q_heads + h) * S;
+  const int tid = threadIdx.x;
+  // lanes of the (possibly partial) warp and the first butterfly offset
+  constexpr unsigned kMask = kThreads >= 32 ? 0xFFFFFFFFu : ((1u << kThreads) - 1u);
+  constexpr int kOff = kThreads >= 32 ? 16 : kThreads / 2;
+  __shared__ float w[1024];  // S <= 1024
+  __shared__ float red[2][(kThreads + 31) / 32];
+  // M = max_s m_s
   float M = -INFINITY;
-  for (int s = 0; s < n; ++s) M = fmaxf(M, a.ws_ml[row0 + s].x);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = tid; s < n; s += kThreads) M = fmaxf(M, a.ws_ml[row0 + s].x);
+#pragma unroll
+  for (int o = kOff; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kMask, M, o));
+  if constexpr (kThreads > 32) {
+    if ((tid & 31) == 0) red[0][tid >> 5] = M;
+    __syncthreads();
+    M = red[0][0];
+    for (int k = 1; k < kThreads / 32; ++k) M = fmaxf(M, red[0][k]);
+  }
+  // w_s and their sum
   float wsum = 0.0f;
-  const int d = threadIdx.x * 4;
-  for (int s = 0; s < n; ++s) {
+  for (int s = tid; s < n; s += kThreads) {
     const float2 ml = a.ws_ml[row0 + s];
-    const float w = (M == -INFINITY) ? 0.0f : ml.y * exp2f(ml.x - M);
-    const float4 o = *reinterpret_cast<const float4*>(a.ws_o + (row0 + s) * D + d);
-    wsum += w;
-    acc.x = fmaf(w, o.x, acc.x);
-    acc.y = fmaf(w, o.y, acc.y);
-    acc.z = fmaf(w, o.z, acc.z);
-    acc.w = fmaf(w, o.w, acc.w);
+    const float ws = (M == -INFINITY) ? 0.0f : ml.y * exp2f(ml.x - M);
+    w[s] = ws;
+    wsum += ws;
+  }
+#pragma unroll
+  for (int o = kOff; o > 0; o >>= 1) wsum += __shfl_xor_sync(kMask, wsum, o);
+  if constexpr (kThreads > 32) {
+    if ((tid & 31) == 0) red[1][tid >> 5] = wsum;
+  }
+  __syncthreads();
+  if constexpr (kThreads > 32) {
+    wsum = red[1][0];
+    for (int k = 1; k < kThreads / 32; ++k) wsum += red[1][k];
+  }
+  // out = sum_s w_s O_s / sum_s w_s
+  const int d = tid * 4;
+  const float* op = a.ws_o + row0 * D + d;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  int s = 0;
+  for (; s + 4 <= n; s += 4) {
+    const float4 o0 = *reinterpret_cast<const float4*>(op + static_cast<int64_t>(s) * D);
+    const float4 o1 = *reinterpret_cast<const float4*>(op + static_cast<int64_t>(s + 1) * D);
+    const float4 o2 = *reinterpret_cast<const float4*>(op + static_cast<int64_t>(s + 2) * D);
+    const float4 o3 = *reinterpret_cast<const float4*>(op + static_cast<int64_t>(s + 3) * D);
+    const float w0 = w[s], w1 = w[s + 1], w2 = w[s + 2], w3 = w[s + 3];
+    acc.x = fmaf(w0, o0.x, fmaf(w1, o1.x, fmaf(w2, o2.x, fmaf(w3, o3.x, acc.x))));
+    acc.y = fmaf(w0, o0.y, fmaf(w1, o1.y, fmaf(w2, o2.y, fmaf(w3, o3.y, acc.y))));
+    acc.z = fmaf(w0, o0.z, fmaf(w1, o1.z, fmaf(w2, o2.z, fmaf(w3, o3.z, acc.z))));
+    acc.w = fmaf(w0, o0.w, fmaf(w1, o1.w, fmaf(w2, o2.w, fmaf(w3, o3.w, acc.w))));
+  }
+  for (; s < n; ++s) {
+    const float4 o = *reinterpret_cast<const float4*>(op + static_cast<int64_t>(s) * D);
+    const float ws = w[s];
+    acc.x = fmaf(ws, o.x, acc.x);
+    acc.y = fmaf(ws, o.y, acc.y);
+    acc.z = fmaf(ws, o.z, acc.z);
+    acc.w = fmaf(ws, o.w, acc.w);
   }
   const float inv = 1.0f / fmaxf(wsum, 1e-20f);
   const uint32_t lo01 = static_cast<uint32_t>(f32_to_bf16(acc.x * inv)) |

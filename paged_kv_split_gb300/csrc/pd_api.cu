@@ -92,6 +92,8 @@ DecodeArgs make_decode_args(const DecodeShape& s, const void* q, const void* kc,
   a.ws_o = static_cast<float*>(ws);
   a.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + ws_o_bytes(s.B, s.Hq, s.D, s.S));
   a.flags = flags;
+  a.out = nullptr;
+  a.direct = 0;
   a.num_blocks = s.nb;
   a.page_bytes = page_bytes_of(s.kv_dtype, s.bs, s.Hkv, s.D);
   a.data_bytes = nvfp4_data_bytes(s.bs, s.Hkv, s.D);
@@ -124,6 +126,7 @@ CombineArgs make_combine_args(int B, int Hq, int D, int bs, int mbs, int S, int 
   c.num_splits = S;
   c.chunk = chunk_pages(page_span_max(mbs, bs, W), S);
   c.sliding_window = W;
+  c.skip_direct = 0;
   return c;
 }
 
@@ -385,13 +388,36 @@ int pd_decode(const void* q, const void* k_cache, const void* v_cache, const int
     S = plan_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, sliding_window,
                     dev->num_sms, mma_ctas_per_sm_estimate(kv_dtype, head_dim));
   }
-  int rc = pd_decode_partial(q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_q_heads,
-                             num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
-                             scale, S, sliding_window, kv_dtype, k_scale, v_scale, workspace,
-                             workspace_bytes, stream);
+  if (use_simple_partial()) {
+    int rc = pd_decode_partial(q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                               num_q_heads, num_kv_heads, head_dim, block_size,
+                               max_blocks_per_seq, num_blocks, scale, S, sliding_window, kv_dtype,
+                               k_scale, v_scale, workspace, workspace_bytes, stream);
+    if (rc != PD_OK || num_seqs == 0) return rc;
+    return pd_decode_combine(workspace, workspace_bytes, seq_lens, out, num_seqs, num_q_heads,
+                             head_dim, block_size, max_blocks_per_seq, S, sliding_window, stream);
+  }
+  // the partial kernel writes the rows of sequences whose keys fit one split
+  // (and zero rows for empty ones); the combine merges the rest
+  const DecodeShape sh{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       max_blocks_per_seq, S, sliding_window, kv_dtype, num_blocks};
+  const int rc = check_decode(sh, q, k_cache, v_cache, block_tables, seq_lens, k_scale, v_scale,
+                              workspace, workspace_bytes);
   if (rc != PD_OK || num_seqs == 0) return rc;
-  return pd_decode_combine(workspace, workspace_bytes, seq_lens, out, num_seqs, num_q_heads,
-                           head_dim, block_size, max_blocks_per_seq, S, sliding_window, stream);
+  if (!isfinite(scale)) return PD_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if (current_device(&dev) != cudaSuccess) return PD_ERR_CUDA;
+  DecodeArgs a = make_decode_args(sh, q, k_cache, v_cache, block_tables, seq_lens, scale, k_scale,
+                                  v_scale, workspace, dev->flags);
+  a.out = static_cast<uint16_t*>(out);
+  a.direct = 1;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_decode_partial_mma(a, head_dim, kv_dtype, st) != cudaSuccess) return PD_ERR_CUDA;
+  CombineArgs c = make_combine_args(num_seqs, num_q_heads, head_dim, block_size,
+                                    max_blocks_per_seq, S, sliding_window, workspace, seq_lens,
+                                    out);
+  c.skip_direct = 1;
+  return cuda_status(launch_decode_combine(c, head_dim, st));
 }
 
 int pd_device_status(int32_t* flags, int32_t reset) {

@@ -121,12 +121,15 @@ __host__ __device__ __forceinline__ int chunk_pages(int span, int S) {
 }
 
 // Workspace: O [B][Hq][S][D] fp32, then ML [B][Hq][S] (m, l) fp32 pairs,
-// the ML region starting on a 256-byte boundary.
+// each region starting on a 256-byte boundary.
 __host__ __device__ __forceinline__ size_t ws_o_bytes(int B, int Hq, int D, int S) {
   return (static_cast<size_t>(B) * Hq * S * D * sizeof(float) + 255) / 256 * 256;
 }
+__host__ __device__ __forceinline__ size_t ws_ml_bytes(int B, int Hq, int S) {
+  return (static_cast<size_t>(B) * Hq * S * 2 * sizeof(float) + 255) / 256 * 256;
+}
 __host__ __device__ __forceinline__ size_t ws_total_bytes(int B, int Hq, int D, int S) {
-  return ws_o_bytes(B, Hq, D, S) + static_cast<size_t>(B) * Hq * S * 2 * sizeof(float);
+  return ws_o_bytes(B, Hq, D, S) + ws_ml_bytes(B, Hq, S);
 }
 
 // ---------------------------------------------------------------------------
@@ -140,6 +143,10 @@ struct DecodeArgs {
   float* ws_o;                   // [B][Hq][S][D]
   float2* ws_ml;                 // [B][Hq][S]
   int* flags;                    // device status word
+  uint16_t* out;                 // [B][Hq][D] bf16 output (used when direct != 0)
+  int direct;                    // 1: a sequence whose keys fit one split writes out
+                                 // itself (and an empty one zero rows); the combine
+                                 // then skips those sequences
   int64_t num_blocks;
   int64_t page_bytes;
   int64_t data_bytes;            // NVFP4 data-section bytes
@@ -155,6 +162,7 @@ struct CombineArgs {
   const int32_t* seq_lens;
   uint16_t* out;
   int num_seqs, num_q_heads, block_size, max_blocks_per_seq, num_splits, chunk, sliding_window;
+  int skip_direct;               // 1: sequences with one key-holding split are already written
 };
 
 // Sequence length as the kernels use it: clamped to the block table, with a

@@ -78,9 +78,33 @@ def test_small_parity(orc, kv_dtype, spec):
     run_parity(orc, case, kv_dtype, [1, 3, 0])
 
 
-def test_many_sequences_unscanned_tickets(orc):
-    """More sequences than the persistent kernel scans in shared memory: its
-    tickets then run over every (sequence, split, kv head), empty ones skipped."""
+def test_two_step_partial_then_combine(orc):
+    """pd_decode_partial + pd_decode_combine (two launches) agree with the oracle
+    like pd_decode (one launch, combine fused into the partial kernel)."""
+    from paged_kv_split_gb300 import binding
+    case = inputs.make_case("twostep", [700, 33, 1290, 0], 32, 8, 128, 16, seed=21)
+    case.block_tables[case.block_tables < 0] = 0
+    kc, vc = U.gpu_write_cache(case, 0)
+    ref, _ = U.oracle_decode(orc, case, kc.cpu().numpy(), vc.cpu().numpy(), 0)
+    q = U.bf16_dev(case.q)
+    bt, lens = U.to_dev(case.block_tables), U.to_dev(case.seq_lens)
+    for S in (1, 4, 9):
+        ws = torch.empty(binding.pd_decode_workspace_bytes(4, 32, 128, S), dtype=torch.uint8,
+                         device="cuda")
+        out = torch.empty_like(q)
+        binding.pd_decode_partial(q, kc, vc, bt, lens, ws, num_kv_heads=8, block_size=16,
+                                  num_blocks=case.num_blocks, scale=case.scale, num_splits=S)
+        binding.pd_decode_combine(ws, lens, out, block_size=16,
+                                  max_blocks_per_seq=case.max_blocks_per_seq, num_splits=S)
+        torch.cuda.synchronize()
+        got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+        U.assert_close(got, ref, what=f"two-step S={S}")
+        fused = U.gpu_decode(case, kc, vc, 0, S)
+        U.assert_close(fused, ref, what=f"fused S={S}")
+
+
+def test_many_sequences(orc):
+    """Over a thousand short sequences, some empty."""
     lens = inputs.uniform_int(77, 1100, 1, 60)
     lens[::97] = 0
     case = inputs.make_case("many", lens, 4, 2, 64, 16, seed=12, extra_blocks=1)
