@@ -38,6 +38,7 @@
 
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "pd_common.cuh"
 
@@ -617,8 +618,10 @@ __global__ void __launch_bounds__(kMmaThreads)
 
       };
       // ---- O^T += V^T P^T for one m-tile (masked keys' V halves zeroed) ----
-      auto pv = [&](const int key0, const uint32_t (&pbf)[NT][2], const uint32_t keep_lo,
-                    const uint32_t keep_hi) {
+      // MASKED: the m-tile is ragged, keep_lo / keep_hi zero the V halves of masked keys
+      auto pv = [&](auto masked, const int key0, const uint32_t (&pbf)[NT][2],
+                    const uint32_t keep_lo, const uint32_t keep_hi) {
+        constexpr bool kMasked = decltype(masked)::value;
         if constexpr (FMT == PD_KV_BF16) {
           const int mi = lane >> 3, ri = lane & 7;
           const int key = key0 + ri + 8 * (mi >> 1);
@@ -628,10 +631,12 @@ __global__ void __launch_bounds__(kMmaThreads)
             const uint32_t off = (d / 64) * (C::kKT * 128) + key * 128 + (d % 64) * 2;
             uint32_t af[4];
             ldsm_x4_trans(vst + swz128(off), af);
-            af[0] &= keep_lo;
-            af[1] &= keep_lo;
-            af[2] &= keep_hi;
-            af[3] &= keep_hi;
+            if constexpr (kMasked) {
+              af[0] &= keep_lo;
+              af[1] &= keep_lo;
+              af[2] &= keep_hi;
+              af[3] &= keep_hi;
+            }
   #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma16816<false>(acc[md][nt], af, pbf[nt][0], pbf[nt][1]);
@@ -662,10 +667,16 @@ __global__ void __launch_bounds__(kMmaThreads)
           for (int md = 0; md < C::kKSteps; ++md) {
             const int jl = md, jh = md + C::kKSteps;
             uint32_t af[4];
-            af[0] = e4m3x2_f16x2(pr01[jl >> 1] >> (16 * (jl & 1))) & keep_lo;
-            af[1] = e4m3x2_f16x2(pr01[jh >> 1] >> (16 * (jh & 1))) & keep_lo;
-            af[2] = e4m3x2_f16x2(pr23[jl >> 1] >> (16 * (jl & 1))) & keep_hi;
-            af[3] = e4m3x2_f16x2(pr23[jh >> 1] >> (16 * (jh & 1))) & keep_hi;
+            af[0] = e4m3x2_f16x2(pr01[jl >> 1] >> (16 * (jl & 1)));
+            af[1] = e4m3x2_f16x2(pr01[jh >> 1] >> (16 * (jh & 1)));
+            af[2] = e4m3x2_f16x2(pr23[jl >> 1] >> (16 * (jl & 1)));
+            af[3] = e4m3x2_f16x2(pr23[jh >> 1] >> (16 * (jh & 1)));
+            if constexpr (kMasked) {
+              af[0] &= keep_lo;
+              af[1] &= keep_lo;
+              af[2] &= keep_hi;
+              af[3] &= keep_hi;
+            }
   #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma16816<true>(acc[md][nt], af, pbf[nt][0], pbf[nt][1]);
@@ -711,10 +722,16 @@ __global__ void __launch_bounds__(kMmaThreads)
   #pragma unroll
           for (int md = 0; md < C::kKSteps; ++md) {
             uint32_t af[4];
-            af[0] = f01[md] & keep_lo;
-            af[1] = f01[md + C::kKSteps] & keep_lo;
-            af[2] = f23[md] & keep_hi;
-            af[3] = f23[md + C::kKSteps] & keep_hi;
+            af[0] = f01[md];
+            af[1] = f01[md + C::kKSteps];
+            af[2] = f23[md];
+            af[3] = f23[md + C::kKSteps];
+            if constexpr (kMasked) {
+              af[0] &= keep_lo;
+              af[1] &= keep_lo;
+              af[2] &= keep_hi;
+              af[3] &= keep_hi;
+            }
   #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma16816<true>(acc[md][nt], af, pbf[nt][0], pbf[nt][1]);
@@ -765,6 +782,14 @@ __global__ void __launch_bounds__(kMmaThreads)
 
       // ---------------- mask, scale, one online-softmax update ----------------
       // fragment rows r (c0,c1) and r+8 (c2,c3) of m-tile u are keys 16*mt + r, +8
+      // an m-tile is ragged if any of its 16 keys is masked (warp-uniform)
+      bool ragged[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int key0 = mt_of(u) * 16;
+        ragged[u] = (t0 + key0 < t_begin) || (t0 + key0 + 16 > t_end) ||
+                    ((bad >> (key0 / C::kBR)) & 1u);
+      }
       float p[kU][NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -772,7 +797,8 @@ __global__ void __launch_bounds__(kMmaThreads)
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
           const int key0 = mt_of(u) * 16;
-          const bool va = key_ok(key0 + r), vb = key_ok(key0 + r + 8);
+          const bool va = !ragged[u] || key_ok(key0 + r);
+          const bool vb = !ragged[u] || key_ok(key0 + r + 8);
           p[u][nt][0] = va ? sc[u][nt][0] * qmul[nt][0] : -INFINITY;
           p[u][nt][1] = va ? sc[u][nt][1] * qmul[nt][1] : -INFINITY;
           p[u][nt][2] = vb ? sc[u][nt][2] * qmul[nt][0] : -INFINITY;
@@ -786,6 +812,8 @@ __global__ void __launch_bounds__(kMmaThreads)
           mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, o));
         }
         const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
+        // the running max of no column moved: every factor is exactly 1, skip the rescale
+        const bool grew = __any_sync(0xFFFFFFFFu, mn0 > m_run[nt][0] || mn1 > m_run[nt][1]);
         const float al0 = (mn0 == -INFINITY) ? 1.0f : ex2(m_run[nt][0] - mn0);
         const float al1 = (mn1 == -INFINITY) ? 1.0f : ex2(m_run[nt][1] - mn1);
         m_run[nt][0] = mn0;
@@ -800,15 +828,19 @@ __global__ void __launch_bounds__(kMmaThreads)
           ls0 += p[u][nt][0] + p[u][nt][2];
           ls1 += p[u][nt][1] + p[u][nt][3];
         }
-        l_run[nt][0] = l_run[nt][0] * al0 + ls0;
-        l_run[nt][1] = l_run[nt][1] * al1 + ls1;
+        if (grew) {
+          l_run[nt][0] *= al0;
+          l_run[nt][1] *= al1;
 #pragma unroll
-        for (int md = 0; md < C::kKSteps; ++md) {
-          acc[md][nt][0] *= al0;
-          acc[md][nt][1] *= al1;
-          acc[md][nt][2] *= al0;
-          acc[md][nt][3] *= al1;
+          for (int md = 0; md < C::kKSteps; ++md) {
+            acc[md][nt][0] *= al0;
+            acc[md][nt][1] *= al1;
+            acc[md][nt][2] *= al0;
+            acc[md][nt][3] *= al1;
+          }
         }
+        l_run[nt][0] += ls0;
+        l_run[nt][1] += ls1;
       }
 
       // ---------------- O^T += V^T P^T, m-tile by m-tile ----------------
@@ -826,16 +858,15 @@ __global__ void __launch_bounds__(kMmaThreads)
           pbf[nt][0] = movmatrix_trans(top);
           pbf[nt][1] = movmatrix_trans(bot);
         }
-        uint32_t keep_lo = 0xFFFFFFFFu, keep_hi = 0xFFFFFFFFu;
-        const bool ragged = (t0 + key0 < t_begin) || (t0 + key0 + 16 > t_end) ||
-                            ((bad >> (key0 / C::kBR)) & 1u);
-        if (ragged) {
-          keep_lo = (key_ok(key0 + 2 * c) ? 0x0000FFFFu : 0u) |
-                    (key_ok(key0 + 2 * c + 1) ? 0xFFFF0000u : 0u);
-          keep_hi = (key_ok(key0 + 2 * c + 8) ? 0x0000FFFFu : 0u) |
-                    (key_ok(key0 + 2 * c + 9) ? 0xFFFF0000u : 0u);
+        if (ragged[u]) {
+          const uint32_t keep_lo = (key_ok(key0 + 2 * c) ? 0x0000FFFFu : 0u) |
+                                   (key_ok(key0 + 2 * c + 1) ? 0xFFFF0000u : 0u);
+          const uint32_t keep_hi = (key_ok(key0 + 2 * c + 8) ? 0x0000FFFFu : 0u) |
+                                   (key_ok(key0 + 2 * c + 9) ? 0xFFFF0000u : 0u);
+          pv(std::true_type{}, key0, pbf, keep_lo, keep_hi);
+        } else {
+          pv(std::false_type{}, key0, pbf, 0u, 0u);
         }
-        pv(key0, pbf, keep_lo, keep_hi);
       }
 
     if constexpr (C::kDSplit == 4) red_buf ^= 1;
