@@ -225,12 +225,36 @@ def time_oracle(case, kv_dtype, kc_host, vc_host, ks, vs, budget_s: float):
         if dt >= budget_s or k >= case.num_seqs:
             break
         k = min(case.num_seqs, max(k + 1, int(k * budget_s / max(dt, 1e-3))))
+    # median of three calls on the chosen sample
+    times = [dt]
+    for _ in range(2):
+        t = time.perf_counter()
+        orc.decode(case.q[:k], kc_host, vc_host, case.block_tables[:k], case.seq_lens[:k],
+                   case.num_kv_heads, case.block_size, case.num_blocks, case.scale,
+                   case.sliding_window, kv_dtype, ks, vs)
+        times.append(time.perf_counter() - t)
+    dt = statistics.median(times)
     sub = type(case)(**{**case.__dict__})
     sub.seq_lens = case.seq_lens[:k]
     sub.num_seqs = k
     sub.q = case.q[:k]
     ab = algorithmic_bytes(sub, kv_dtype)
     return k, dt, ab
+
+
+def cpu_description() -> dict:
+    """Host CPU model and core count (the oracle baseline runs on one core)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return {"nproc": os.cpu_count(), "model": model or platform.processor() or platform.machine()}
 
 
 def build_device_state(case, kv_dtype, replicas, dev):
@@ -342,6 +366,63 @@ def run_pd(args, rank, world, local):
     torch.cuda.synchronize(dev)
     partial_ms = [a.elapsed_time(b) for a, b in evs]
 
+    # per-step spread of the whole decode step (events around each pd_decode)
+    n_dist = min(args.steps, 500)
+    evd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_dist)]
+    for i in range(n_dist):
+        evd[i][0].record(stream)
+        step(i)
+        evd[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    step_us = np.array([a.elapsed_time(b) * 1e3 for a, b in evd])
+    spread = {f"p{p}": round(float(np.percentile(step_us, p)), 2) for p in (10, 50, 90)}
+
+    # the same step captured in CUDA graphs (one per cache replica), replayed in rotation
+    def timed_replays(graphs, n):
+        for i in range(3):
+            graphs[i % len(graphs)].replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            graphs[i % len(graphs)].replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) * 1e3 / n
+
+    n_graph = min(args.steps, 2000)
+    graphs = []
+    for rep_i in range(replicas):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(rep_i)
+        graphs.append(g)
+    graph_us = timed_replays(graphs, n_graph)
+
+    # a serving step: write one new token per sequence (its K and V), then
+    # decode, both in one graph; the write lands on each sequence's last slot
+    L = case.seq_lens.astype(np.int64)
+    last_slot = (case.block_tables[np.arange(B), np.maximum(L - 1, 0) // case.block_size]
+                 .astype(np.int64) * case.block_size + np.maximum(L - 1, 0) % case.block_size)
+    from paged_kv_split_gb300 import inputs as I
+    new_k = torch.from_numpy(I.normal_bf16(77, (B, case.num_kv_heads, D)).view(np.int16)).to(
+        dev).view(torch.bfloat16)
+    new_v = torch.from_numpy(I.normal_bf16(78, (B, case.num_kv_heads, D)).view(np.int16)).to(
+        dev).view(torch.bfloat16)
+    slots_new = torch.from_numpy(np.where(L > 0, last_slot, -1).astype(np.int32)).to(dev)
+    graphs_w = []
+    for rep_i in range(replicas):
+        kc, vc = caches[rep_i]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            pd.pd_reshape_and_cache(new_k, new_v, kc, vc, slots_new, num_blocks=case.num_blocks,
+                                    block_size=case.block_size, kv_dtype=kv_dtype, k_scale=ks,
+                                    v_scale=vs)
+            pd.pd_decode(q, kc, vc, bt, lens, out, workspace=ws, **common)
+        graphs_w.append(g)
+    graph_w_us = timed_replays(graphs_w, n_graph)
+
     ms_step_local = total_ms / args.steps
     ms_step = max_over_ranks(ms_step_local, world)
     total_bytes = sum_over_ranks(ab["total"], world)
@@ -396,6 +477,7 @@ def run_pd(args, rank, world, local):
                                  args.cpu_budget)
         cpu = {"value": round(sab["total"] / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
                "kind": "oracle", "us_per_step_sample": round(dt * 1e6, 1),
+               "host": cpu_description(), "timing": "median of 3 calls",
                "sample": f"first {k} of {case.num_seqs} sequences of the same batch "
                          f"({sab['keys']} keys), one single-threaded oracle_decode call"}
 
@@ -418,6 +500,14 @@ def run_pd(args, rank, world, local):
                              f"{2 * cache_bytes / 1e6:.0f} MB rotated per step "
                              f"(L2 {l2 / 1e6:.0f} MB)",
                        "parallelism": f"replicas x{world}"},
+            "step_us": spread,
+            "graph": {"us_per_step": round(graph_us, 2),
+                      "value": round(ab["total"] / (graph_us * 1e-6) / 1e9, 1), "unit": "GB/s",
+                      "note": "pd_decode captured in one CUDA graph per cache replica"},
+            "graph_with_write": {"us_per_step": round(graph_w_us, 2),
+                                 "tokens_written": int(B),
+                                 "note": "pd_reshape_and_cache of one token per sequence, then "
+                                         "pd_decode, captured in one CUDA graph"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": 2 * args.steps, "clocks": clocks,
         }

@@ -317,6 +317,22 @@ __global__ void __launch_bounds__(kMmaThreads)
   const int r = lane >> 2;  // fragment row group
   const int c = lane & 3;   // fragment column pair
 
+  // Without a window the split's first page does not depend on the sequence
+  // length, so the producer loads its block-table entries (and prefetches the
+  // tensor maps) while the length is still in flight.
+  const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
+  int spec_entry = -1;
+  if (warp == kConsumerWarps && a.sliding_window == 0) {
+    if constexpr (FMT != PD_KV_NVFP4) {
+      if (lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
+      }
+    }
+    const int e = s * a.chunk + lane;
+    if (e < a.max_blocks_per_seq) spec_entry = bt[e];
+  }
+
   // ---- the split's key range ----
   int L = a.seq_lens[b];
   {
@@ -363,12 +379,11 @@ __global__ void __launch_bounds__(kMmaThreads)
   }
   __syncthreads();
 
-  const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
-
   // =========================== producer warp ===============================
   if (warp == kConsumerWarps) {
-    int cached_base = -(1 << 30);
-    int my_entry = -1;
+    // entries [cached_base, cached_base + 32) of the block-table row, one per lane
+    int cached_base = a.sliding_window == 0 ? s * a.chunk : -(1 << 30);
+    int my_entry = spec_entry;
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % C::kStages;
       if (i >= C::kStages &&

@@ -169,6 +169,39 @@ def make_case(name, seq_lens, num_q_heads, num_kv_heads, head_dim, block_size, *
                 kv_dtype=kv_dtype)
 
 
+@dataclass
+class DecodeStep:
+    """The inputs of one decode step that appends a token to every sequence."""
+    q: np.ndarray             # uint16 bf16 bits [B, Hq, D]
+    key: np.ndarray           # uint16 bf16 bits [B, Hkv, D], the new token's K
+    value: np.ndarray         # uint16 bf16 bits [B, Hkv, D], the new token's V
+    slot_mapping: np.ndarray  # int32 [B], slot of the new token
+    seq_lens: np.ndarray      # int32 [B], lengths including the new token
+
+
+def decode_steps(case: Case, steps: int, seed: int = 0) -> list:
+    """`steps` decode steps over `case`, whose lengths are the lengths after
+    the last step: step i appends position L_b - steps + i of sequence b
+    (its page is already in the block table) and attends over L_b - steps +
+    i + 1 keys. Sequences shorter than `steps` are not allowed."""
+    B = case.num_seqs
+    L_final = case.seq_lens.astype(np.int64)
+    if B and int(L_final.min()) < steps:
+        raise ValueError("every sequence needs at least `steps` tokens")
+    bs = case.block_size
+    out = []
+    for i in range(steps):
+        pos = L_final - steps + i
+        page = case.block_tables[np.arange(B), pos // bs].astype(np.int64)
+        slots = (page * bs + pos % bs).astype(np.int32)
+        out.append(DecodeStep(
+            q=normal_bf16(seed + 100 + 3 * i, (B, case.num_q_heads, case.head_dim)),
+            key=normal_bf16(seed + 101 + 3 * i, (B, case.num_kv_heads, case.head_dim)),
+            value=normal_bf16(seed + 102 + 3 * i, (B, case.num_kv_heads, case.head_dim)),
+            slot_mapping=slots, seq_lens=(pos + 1).astype(np.int32)))
+    return out
+
+
 # ---- the named workloads -------------------------------------------------
 def tiny(num_splits: int = 1, seed: int = 0) -> Case:
     """2 seqs {17, 40}, 4 q / 2 kv heads, D=64, bs=16, a 16-page pool."""
