@@ -1,14 +1,17 @@
 """Decode benchmark: paged split-KV decode attention on GB300.
 
-One step = one pd_decode (split-KV partial kernel + log-sum-exp combine) over the
-whole batch of the Llama-3-8B-shaped workload (32 sequences, 32 q / 8 kv
-heads, head_dim 128, block_size 16, lengths uniform in [1024, 4096], BF16
-cache, pages shuffled across the pool, splits from the length-aware planner), inputs
-resident in HBM. Reported value: KV-read GB/s = algorithmic bytes / step time
-(us/step alongside); e2e: the same through the C ABI from pinned host inputs.
+One step = one decode (partial kernel + log-sum-exp combine) over the whole
+batch of the Llama-3-8B-shaped workload (32 sequences, 32 q / 8 kv heads,
+head_dim 128, block_size 16, lengths uniform in [1024, 4096], BF16 cache, pages
+shuffled across the pool), inputs resident in HBM. The schedule comes from the
+host-held lengths: pd_prefer_balanced picks between pd_decode with the
+length-aware split count and pd_decode_balanced with a host plan. Reported
+value: KV-read GB/s = algorithmic bytes / step time (us/step alongside); e2e:
+the same through the C ABI from pinned host inputs, planning included.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pd|reference]
                     [--workload llama8b|long_b4_32k|...] [--splits S]
+                    [--schedule auto|split|balanced]
 
 With torchrun (N > 1) every rank decodes its own independent batch (seeded by
 rank, replicas only: no data is exchanged); the barrier and max-over-ranks
@@ -36,6 +39,7 @@ METRIC = "decode µs/step and KV-read HBM GB/s (% of GB300 peak) at 1 GPU"
 ELEM_BYTES = {0: 2.0, 1: 1.0, 2: 0.5625}
 DTYPE_NAME = {0: "bf16", 1: "fp8_e4m3", 2: "nvfp4"}
 PARTIAL_KERNEL_SRC = ["paged_kv_split_gb300/csrc/decode_mma.cu",
+                      "paged_kv_split_gb300/csrc/decode_balanced.cu",
                       "paged_kv_split_gb300/csrc/pd_common.cuh"]
 
 
@@ -306,30 +310,79 @@ def run_pd(args, rank, world, local):
     # the host holds the batch's lengths (as a serving scheduler does), so the
     # split count comes from the length-aware planner unless one is given
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    S = args.splits or pd.pd_plan_num_splits_for_lengths(
-        case.seq_lens, hq, case.num_kv_heads, mbs, case.block_size, case.sliding_window, D,
-        kv_dtype, sms)
-    ws = torch.empty(pd.pd_decode_workspace_bytes(B, hq, D, S), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    common = dict(num_kv_heads=case.num_kv_heads, block_size=case.block_size,
-                  num_blocks=case.num_blocks, scale=case.scale, num_splits=S,
-                  sliding_window=case.sliding_window, kv_dtype=kv_dtype, k_scale=ks, v_scale=vs)
+    G = hq // case.num_kv_heads
+    kw = dict(num_kv_heads=case.num_kv_heads, block_size=case.block_size,
+              num_blocks=case.num_blocks, scale=case.scale, sliding_window=case.sliding_window,
+              kv_dtype=kv_dtype, k_scale=ks, v_scale=vs)
+    # the host holds the batch's lengths (as a serving scheduler does): the
+    # schedule (split-KV with the length-aware split count, or the balanced
+    # plan) is chosen and planned from them
+    schedule = args.schedule
+    if schedule == "auto":
+        schedule = "balanced" if (not args.splits and pd.pd_prefer_balanced(
+            case.seq_lens, num_q_heads=hq, num_kv_heads=case.num_kv_heads,
+            max_blocks_per_seq=mbs, block_size=case.block_size, head_dim=D,
+            sliding_window=case.sliding_window, kv_dtype=kv_dtype, num_sms=sms)) else "split"
+    if schedule == "balanced":
+        def make_plan(out_buf=None):
+            return pd.pd_balanced_plan(case.seq_lens, num_q_heads=hq,
+                                       num_kv_heads=case.num_kv_heads, head_dim=D,
+                                       block_size=case.block_size, max_blocks_per_seq=mbs,
+                                       sliding_window=case.sliding_window, kv_dtype=kv_dtype,
+                                       num_sms=sms, out=out_buf)
+        plan = make_plan()
+        plan_d = plan.to(dev)
+        ws = torch.zeros(max(plan.workspace_bytes, 16), dtype=torch.uint8, device=dev)
+        S = None
+        sched_cfg = {"schedule": "balanced (host plan)", "plan_ctas": plan.num_ctas,
+                     "plan_pieces": plan.num_pieces}
+        ws_traffic = 2 * plan.num_pieces * G * (D + 2) * 4
+
+        def decode(kc, vc, q_, bt_, lens_, out_, plan_dev=None):
+            pd.pd_decode_balanced(q_, kc, vc, bt_, plan_d if plan_dev is None else plan_dev,
+                                  plan, out_, workspace=ws, **kw)
+
+        def partial_only(kc, vc):
+            pd.pd_decode_balanced_partial(q, kc, vc, bt, plan_d, plan, out, workspace=ws, **kw)
+
+        def combine_only(kc, vc):
+            pd.pd_decode_balanced_combine(q, kc, vc, bt, plan_d, plan, out, workspace=ws, **kw)
+    else:
+        S = args.splits or pd.pd_plan_num_splits_for_lengths(
+            case.seq_lens, hq, case.num_kv_heads, mbs, case.block_size, case.sliding_window, D,
+            kv_dtype, sms)
+        ws = torch.empty(pd.pd_decode_workspace_bytes(B, hq, D, S), dtype=torch.uint8,
+                         device=dev)
+        sched_cfg = {"schedule": "split-KV", "num_splits": S,
+                     "split_planner": "given" if args.splits else "seq_lens"}
+        ws_traffic = 2 * B * hq * S * (D + 2) * 4
+
+        def decode(kc, vc, q_, bt_, lens_, out_, plan_dev=None):
+            pd.pd_decode(q_, kc, vc, bt_, lens_, out_, workspace=ws, num_splits=S, **kw)
+
+        def partial_only(kc, vc):
+            pd.pd_decode_partial(q, kc, vc, bt, lens, ws, num_splits=S, **kw)
+
+        def combine_only(kc, vc):
+            pd.pd_decode_combine(ws, lens, out, block_size=case.block_size,
+                                 max_blocks_per_seq=mbs, num_splits=S,
+                                 sliding_window=case.sliding_window)
 
     def step(i):
-        # one decode step = one pd_decode (the partial kernel, then the combine
-        # launched as its programmatic dependent)
+        # one decode step = the partial kernel, then the combine launched as
+        # its programmatic dependent
         kc, vc = caches[i % replicas]
-        pd.pd_decode(q, kc, vc, bt, lens, out, workspace=ws, **common)
+        decode(kc, vc, q, bt, lens, out)
 
     def split_step(i, ev):
         # the same two kernels launched separately, with events around the
-        # split-KV partial kernel (the roofline's kernel)
+        # partial kernel (the roofline's kernel)
         kc, vc = caches[i % replicas]
         ev[0].record(stream)
-        pd.pd_decode_partial(q, kc, vc, bt, lens, ws, **common)
+        partial_only(kc, vc)
         ev[1].record(stream)
-        pd.pd_decode_combine(ws, lens, out, block_size=case.block_size, max_blocks_per_seq=mbs,
-                             num_splits=S, sliding_window=case.sliding_window)
+        combine_only(kc, vc)
 
     for i in range(args.warmup):
         step(i)
@@ -419,7 +472,7 @@ def run_pd(args, rank, world, local):
             pd.pd_reshape_and_cache(new_k, new_v, kc, vc, slots_new, num_blocks=case.num_blocks,
                                     block_size=case.block_size, kv_dtype=kv_dtype, k_scale=ks,
                                     v_scale=vs)
-            pd.pd_decode(q, kc, vc, bt, lens, out, workspace=ws, **common)
+            decode(kc, vc, q, bt, lens, out)
         graphs_w.append(g)
     graph_w_us = timed_replays(graphs_w, n_graph)
 
@@ -433,7 +486,8 @@ def run_pd(args, rank, world, local):
     partial_bytes = ab["kv"] + ab["q"] + ab["table"]
     peak, peak_kind = measured_peaks()
     achieved = partial_bytes / (part_ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "split-KV partial", "achieved": round(achieved, 1),
+    roofline = {"bound": "hbm", "kernel": "partial (" + sched_cfg["schedule"] + ")",
+                "achieved": round(achieved, 1),
                 "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(args.workload),
                 "algorithmic_bytes_per_launch": int(partial_bytes),
@@ -447,13 +501,24 @@ def run_pd(args, rank, world, local):
     out_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
     q_d, bt_d, lens_d = torch.empty_like(q), torch.empty_like(bt), torch.empty_like(lens)
     e2e_steps = max(10, min(args.steps, 200))
+    plan_bytes = 0
+    if schedule == "balanced":
+        plan_h = pd.balanced_plan_buffer(B, case.num_kv_heads, sms, pin=True)
+        plan_dd = torch.empty_like(plan_d)
+        plan_bytes = plan_d.numel() * 4
 
     def e2e_step(i):
         kc, vc = caches[i % replicas]
         q_d.copy_(q_h, non_blocking=True)
         bt_d.copy_(bt_h, non_blocking=True)
         lens_d.copy_(lens_h, non_blocking=True)
-        pd.pd_decode(q_d, kc, vc, bt_d, lens_d, out, workspace=ws, **common)
+        if schedule == "balanced":
+            # the scheduler plans every step (lengths change as tokens arrive)
+            make_plan(plan_h)  # plans straight into the pinned buffer
+            plan_dd.copy_(plan_h, non_blocking=True)
+            decode(kc, vc, q_d, bt_d, lens_d, out, plan_dev=plan_dd)
+        else:
+            decode(kc, vc, q_d, bt_d, lens_d, out)
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()
 
@@ -464,7 +529,7 @@ def run_pd(args, rank, world, local):
     for i in range(e2e_steps):
         e2e_step(i)
     e2e_s = max_over_ranks((time.perf_counter() - t) / e2e_steps, world)
-    h2d = q_h.numel() * 2 + bt_h.numel() * 4 + lens_h.numel() * 4
+    h2d = q_h.numel() * 2 + bt_h.numel() * 4 + lens_h.numel() * 4 + plan_bytes
     d2h = out_h.numel() * 2
     e2e = {"value": round(total_bytes / e2e_s / 1e9, 1), "unit": "GB/s",
            "us_per_step": round(e2e_s * 1e6, 2), "h2d_bytes_per_step": int(h2d),
@@ -492,10 +557,9 @@ def run_pd(args, rank, world, local):
             "config": {"workload": args.workload, "num_seqs": B, "num_q_heads": hq,
                        "num_kv_heads": case.num_kv_heads, "head_dim": D,
                        "block_size": case.block_size, "kv_dtype": DTYPE_NAME[kv_dtype],
-                       "sliding_window": case.sliding_window, "num_splits": S,
-                       "split_planner": "given" if args.splits else "seq_lens",
+                       "sliding_window": case.sliding_window, **sched_cfg,
                        "keys_per_step": ab["keys"], "algorithmic_bytes_per_step": int(ab["total"]),
-                       "workspace_bytes_per_step": int(2 * B * hq * S * (D + 2) * 4),
+                       "workspace_bytes_per_step": int(ws_traffic),
                        "l2": f"inputs larger than L2: {replicas} cache replicas of "
                              f"{2 * cache_bytes / 1e6:.0f} MB rotated per step "
                              f"(L2 {l2 / 1e6:.0f} MB)",
@@ -570,6 +634,7 @@ def main():
     ap.add_argument("--impl", default="pd", choices=["pd", "reference"])
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--schedule", default="auto", choices=["auto", "split", "balanced"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -72,7 +72,8 @@ enum pd_device_flag {
   PD_DEV_BAD_PAGE = 1,    /* a block_tables entry was < 0 or >= num_blocks: page skipped */
   PD_DEV_BAD_SEQ_LEN = 2, /* seq_lens[b] < 0 or > max_blocks_per_seq*block_size: clamped */
   PD_DEV_BAD_SLOT = 4,    /* slot_mapping[t] >= num_blocks*block_size: token skipped */
-  PD_DEV_TIMEOUT = 8      /* a bounded wait inside a kernel gave up: that output is invalid */
+  PD_DEV_TIMEOUT = 8,     /* a bounded wait inside a kernel gave up: that output is invalid */
+  PD_DEV_BAD_PLAN = 16    /* a balanced-plan entry was out of range: that piece skipped */
 };
 
 /* Human-readable name of a pd_status value (static string, never NULL). */
@@ -207,6 +208,94 @@ int pd_decode_combine(const void* workspace, size_t workspace_bytes, const int32
                       void* out, int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                       int32_t block_size, int32_t max_blocks_per_seq, int32_t num_splits,
                       int32_t sliding_window, void* stream);
+
+/* ---- Balanced decode: a host-made plan that gives every CTA equal work ----
+ *
+ * pd_decode splits every sequence into the same S splits, so CTAs get unequal
+ * work when lengths differ and the grid runs in several generations. A
+ * serving scheduler already holds the lengths on the host; from them
+ * pd_balanced_plan cuts the line of all (sequence, kv head) key ranges, laid
+ * end to end in sequence-major order, into one equal share of pages per
+ * resident CTA (the split-KV partition of [metrale] `paged_decode_attn_splitk_*`
+ * with per-head, length-dependent split points). A share that crosses a head's
+ * range boundary holds several "pieces"; each piece gets its own partial
+ * (O, m, l), merged by the same log-sum-exp combine ([metrale]
+ * `paged_decode_attn_reduce_*`). Results equal pd_decode's up to fp32
+ * summation order. */
+
+/* Which schedule to run for these host lengths: 1 if the balanced one is
+ * expected to be faster than pd_decode with pd_plan_num_splits_for_lengths'
+ * split count, 0 if not, a negative pd_status on bad arguments. Host only.
+ * It compares the split planner's estimated makespan with an equal share per
+ * CTA plus a measured per-tile premium of the balanced kernel (about 5 %) and
+ * its per-piece cost: lengths that differ favour the balanced schedule,
+ * equal lengths the split one. */
+int pd_prefer_balanced(const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t max_blocks_per_seq, int32_t block_size,
+                       int32_t sliding_window, int32_t head_dim, int32_t kv_dtype,
+                       int32_t num_sms);
+
+/* Upper bound of the plan bytes for num_seqs sequences, num_kv_heads heads and
+ * a device with num_sms SMs (host only). */
+size_t pd_balanced_plan_bytes(int32_t num_seqs, int32_t num_kv_heads, int32_t num_sms);
+
+/* Build the plan on the host from host seq_lens[num_seqs] (clamped to
+ * [0, max_blocks_per_seq * block_size], windowed like pd_decode).
+ *   plan          host buffer, 16-byte aligned, of plan_bytes >=
+ *                 pd_balanced_plan_bytes; copy it to the device before
+ *                 pd_decode_balanced (its bytes, as written, are the device
+ *                 plan). The plan is valid only for these lengths: build a new
+ *                 one whenever a length changes.
+ *   num_ctas, num_pieces  out: pass them to pd_decode_balanced.
+ *   workspace_bytes       out: the workspace pd_decode_balanced needs.
+ * Returns PD_OK, PD_ERR_INVALID_ARG / PD_ERR_UNSUPPORTED on bad shapes, or
+ * PD_ERR_WORKSPACE_TOO_SMALL if plan_bytes is short. No CUDA call. */
+int pd_balanced_plan(const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                     int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                     int32_t max_blocks_per_seq, int32_t sliding_window, int32_t kv_dtype,
+                     int32_t num_sms, void* plan, size_t plan_bytes, int32_t* num_ctas,
+                     int32_t* num_pieces, size_t* workspace_bytes);
+
+/* One decode step over a balanced plan: the partial kernel (one CTA per plan
+ * share, pieces in order; a head covered by one piece is written to out
+ * directly) and then the combine, which also writes the zero rows of empty
+ * sequences. Arguments as pd_decode, with
+ *   plan, plan_bytes       the device copy of pd_balanced_plan's output.
+ *   num_ctas, num_pieces   pd_balanced_plan's outputs for that plan.
+ *   workspace              device scratch of >= the planner's workspace_bytes;
+ *                          contents on entry do not matter.
+ * seq_lens is not an argument: the plan carries each piece's key range.
+ * Plan entries out of range are skipped and raise PD_DEV_BAD_PLAN in the
+ * device status word. No allocation, no synchronisation. */
+int pd_decode_balanced(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const void* plan, size_t plan_bytes,
+                       void* out, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
+                       int64_t num_blocks, float scale, int32_t sliding_window,
+                       int32_t kv_dtype, float k_scale, float v_scale, int32_t num_ctas,
+                       int32_t num_pieces, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/* The two halves of pd_decode_balanced, with its arguments: the partial
+ * kernel alone (writes the workspace partials and the rows of heads one
+ * piece covers), then the combine alone (reads the same workspace and plan).
+ * For timing each kernel on its own; pd_decode_balanced launches both. */
+int pd_decode_balanced_partial(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const void* plan, size_t plan_bytes,
+                               void* out, int32_t num_seqs, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
+                               int32_t sliding_window, int32_t kv_dtype, float k_scale,
+                               float v_scale, int32_t num_ctas, int32_t num_pieces,
+                               void* workspace, size_t workspace_bytes, void* stream);
+int pd_decode_balanced_combine(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const void* plan, size_t plan_bytes,
+                               void* out, int32_t num_seqs, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
+                               int32_t sliding_window, int32_t kv_dtype, float k_scale,
+                               float v_scale, int32_t num_ctas, int32_t num_pieces,
+                               void* workspace, size_t workspace_bytes, void* stream);
 
 /* Size of the workspace array that pd_decode_static_ws uses (8 MiB). */
 #define PD_STATIC_WORKSPACE_BYTES (8u << 20)

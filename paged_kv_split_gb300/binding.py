@@ -54,6 +54,20 @@ _lib.pd_decode_partial.restype = ctypes.c_int
 _lib.pd_decode_combine.argtypes = [_P, _sz, _P, _P, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _P]
 _lib.pd_decode_combine.restype = ctypes.c_int
 _lib.pd_device_status.argtypes, _lib.pd_device_status.restype = [_P, _i32], ctypes.c_int
+_lib.pd_prefer_balanced.argtypes = [_P, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]
+_lib.pd_prefer_balanced.restype = ctypes.c_int
+_lib.pd_balanced_plan_bytes.argtypes = [_i32, _i32, _i32]
+_lib.pd_balanced_plan_bytes.restype = _sz
+_lib.pd_balanced_plan.argtypes = [_P, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _P,
+                                  _sz, _P, _P, _P]
+_lib.pd_balanced_plan.restype = ctypes.c_int
+_lib.pd_decode_balanced.argtypes = [_P, _P, _P, _P, _P, _sz, _P, _i32, _i32, _i32, _i32, _i32,
+                                    _i32, _i64, _f32, _i32, _i32, _f32, _f32, _i32, _i32, _P,
+                                    _sz, _P]
+_lib.pd_decode_balanced.restype = ctypes.c_int
+for _fn in ("pd_decode_balanced_partial", "pd_decode_balanced_combine"):
+    getattr(_lib, _fn).argtypes = _lib.pd_decode_balanced.argtypes
+    getattr(_lib, _fn).restype = ctypes.c_int
 
 
 class PdError(RuntimeError):
@@ -262,3 +276,102 @@ def pd_device_status(reset: bool = False) -> int:
     v = ctypes.c_int32(0)
     _check("pd_device_status", _lib.pd_device_status(ctypes.addressof(v), int(bool(reset))))
     return int(v.value)
+
+
+# ---- balanced decode -------------------------------------------------------
+class BalancedPlan:
+    """A host plan from pd_balanced_plan: `host` (CPU int32 tensor whose bytes
+    are the device plan), `num_ctas`, `num_pieces`, `workspace_bytes`."""
+
+    def __init__(self, host, num_ctas, num_pieces, workspace_bytes):
+        self.host = host
+        self.num_ctas = num_ctas
+        self.num_pieces = num_pieces
+        self.workspace_bytes = workspace_bytes
+
+    @property
+    def words(self):
+        """The plan as a numpy int32 array (a view of `host`)."""
+        return self.host.numpy()
+
+    def to(self, device):
+        """The plan as a device int32 tensor (what pd_decode_balanced reads)."""
+        return self.host.to(device)
+
+
+def balanced_plan_buffer(num_seqs, num_kv_heads, num_sms, pin=False):
+    """A host int32 buffer large enough for any plan of these shapes."""
+    nbytes = int(_lib.pd_balanced_plan_bytes(num_seqs, num_kv_heads, num_sms))
+    if nbytes == 0:
+        raise ValueError("bad plan shape")
+    buf = torch.zeros((nbytes + 15) // 16 * 4, dtype=torch.int32)
+    return buf.pin_memory() if pin else buf
+
+
+def pd_balanced_plan(seq_lens_host, *, num_q_heads, num_kv_heads, head_dim, block_size,
+                     max_blocks_per_seq, sliding_window=0, kv_dtype=PD_KV_BF16, num_sms,
+                     out=None):
+    """Build a balanced plan on the host from host lengths (int32 [B], numpy or
+    CPU tensor). `out`: a buffer from balanced_plan_buffer to plan into (it is
+    reused, so a scheduler can plan every step without allocating)."""
+    import numpy as np
+    lens = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
+    B = int(lens.shape[0])
+    if out is None:
+        out = balanced_plan_buffer(B, num_kv_heads, num_sms)
+    nc, npc, wsb = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_size_t(0)
+    rc = _lib.pd_balanced_plan(lens.ctypes.data if B else None, B, num_q_heads, num_kv_heads,
+                               head_dim, block_size, max_blocks_per_seq, sliding_window,
+                               _dtype_code(kv_dtype), num_sms, out.data_ptr(),
+                               out.numel() * 4, ctypes.byref(nc), ctypes.byref(npc),
+                               ctypes.byref(wsb))
+    _check("pd_balanced_plan", rc)
+    return BalancedPlan(out, nc.value, npc.value, wsb.value)
+
+
+def pd_decode_balanced(q, k_cache, v_cache, block_tables, plan_dev, plan, out, *, num_kv_heads,
+                       block_size, num_blocks, scale, sliding_window=0, kv_dtype=PD_KV_BF16,
+                       k_scale=1.0, v_scale=1.0, workspace=None, stream=None, _fn="pd_decode_balanced"):
+    """One balanced decode step into out; plan_dev is plan.to(device)."""
+    B, hq, d = q.shape
+    if block_tables.dim() != 2 or block_tables.shape[0] != B:
+        raise ValueError("block_tables must be [num_seqs, max_blocks_per_seq]")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    mbs = block_tables.shape[1]
+    dev = q.device
+    if workspace is None:
+        workspace = torch.empty(max(plan.workspace_bytes, 16), dtype=torch.uint8, device=dev)
+    rc = getattr(_lib, _fn)(
+        _dev(q, "q", torch.bfloat16, dev), _dev(k_cache, "k_cache", None, dev),
+        _dev(v_cache, "v_cache", None, dev), _dev(block_tables, "block_tables", torch.int32, dev),
+        _dev(plan_dev, "plan", torch.int32, dev), plan_dev.numel() * 4,
+        _dev(out, "out", torch.bfloat16, dev), B, hq, num_kv_heads, d, block_size, mbs,
+        num_blocks, float(scale), sliding_window, _dtype_code(kv_dtype), float(k_scale),
+        float(v_scale), plan.num_ctas, plan.num_pieces, _dev(workspace, "workspace", None, dev),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(_fn, rc)
+    return out
+
+
+def pd_decode_balanced_partial(*args, **kw):
+    """The partial kernel of pd_decode_balanced alone (same arguments)."""
+    return pd_decode_balanced(*args, _fn="pd_decode_balanced_partial", **kw)
+
+
+def pd_decode_balanced_combine(*args, **kw):
+    """The combine kernel of pd_decode_balanced alone (same arguments)."""
+    return pd_decode_balanced(*args, _fn="pd_decode_balanced_combine", **kw)
+
+
+def pd_prefer_balanced(seq_lens_host, *, num_q_heads, num_kv_heads, max_blocks_per_seq,
+                       block_size, head_dim, sliding_window=0, kv_dtype=PD_KV_BF16, num_sms):
+    """True if the balanced schedule is expected faster for these host lengths."""
+    import numpy as np
+    lens = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
+    r = _lib.pd_prefer_balanced(lens.ctypes.data if lens.size else None, int(lens.shape[0]),
+                                num_q_heads, num_kv_heads, max_blocks_per_seq, block_size,
+                                sliding_window, head_dim, _dtype_code(kv_dtype), num_sms)
+    if r < 0:
+        raise PdError("pd_prefer_balanced", -r)
+    return bool(r)

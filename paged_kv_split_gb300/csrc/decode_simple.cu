@@ -175,14 +175,29 @@ __global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
   constexpr int kThreads = D / 4;
   const int h = blockIdx.x;
   const int b = blockIdx.y;
-  const int S = a.num_splits;
-  int L = a.seq_lens[b];
-  const int cap = a.max_blocks_per_seq * a.block_size;
-  L = L < 0 ? 0 : (L > cap ? cap : L);
-  const int P = num_key_pages(L, a.sliding_window, a.block_size);
-  const int n = min((P + a.chunk - 1) / a.chunk, S);  // splits holding keys
-  if (a.skip_direct && n <= 1) return;  // the partial kernel wrote this row
-  const int64_t row0 = (static_cast<int64_t>(b) * a.num_q_heads + h) * S;
+  // partial s of this (sequence, q head) is workspace row row0 + s * stride
+  int n;
+  int64_t row0;
+  int stride;
+  if (a.plan_seg != nullptr) {
+    // balanced plan: the pieces of this q head's kv head, consecutive slots
+    const int G = a.num_q_heads / a.num_kv_heads;
+    const int g = h / G;
+    const int64_t e = 2 * (static_cast<int64_t>(b) * a.num_kv_heads + g);
+    n = a.plan_seg[e + 1];
+    if (n == 1) return;  // one piece: the partial kernel wrote this row
+    row0 = static_cast<int64_t>(a.plan_seg[e]) * G + (h - g * G);
+    stride = G;
+  } else {
+    int L = a.seq_lens[b];
+    const int cap = a.max_blocks_per_seq * a.block_size;
+    L = L < 0 ? 0 : (L > cap ? cap : L);
+    const int P = num_key_pages(L, a.sliding_window, a.block_size);
+    n = min((P + a.chunk - 1) / a.chunk, a.num_splits);  // splits holding keys
+    if (a.skip_direct && n <= 1) return;  // the partial kernel wrote this row
+    row0 = (static_cast<int64_t>(b) * a.num_q_heads + h) * a.num_splits;
+    stride = 1;
+  }
   const int tid = threadIdx.x;
   // lanes of the (possibly partial) warp and the first butterfly offset
   constexpr unsigned kMask = kThreads >= 32 ? 0xFFFFFFFFu : ((1u << kThreads) - 1u);
@@ -191,7 +206,7 @@ __global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
   __shared__ float red[2][(kThreads + 31) / 32];
   // M = max_s m_s
   float M = -INFINITY;
-  for (int s = tid; s < n; s += kThreads) M = fmaxf(M, a.ws_ml[row0 + s].x);
+  for (int s = tid; s < n; s += kThreads) M = fmaxf(M, a.ws_ml[row0 + s * stride].x);
 #pragma unroll
   for (int o = kOff; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kMask, M, o));
   if constexpr (kThreads > 32) {
@@ -203,7 +218,7 @@ __global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
   // w_s and their sum
   float wsum = 0.0f;
   for (int s = tid; s < n; s += kThreads) {
-    const float2 ml = a.ws_ml[row0 + s];
+    const float2 ml = a.ws_ml[row0 + s * stride];
     const float ws = (M == -INFINITY) ? 0.0f : ml.y * exp2f(ml.x - M);
     w[s] = ws;
     wsum += ws;
@@ -221,13 +236,14 @@ __global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
   // out = sum_s w_s O_s / sum_s w_s
   const int d = tid * 4;
   const float* op = a.ws_o + row0 * D + d;
+  const int64_t ostep = static_cast<int64_t>(stride) * D;  // between consecutive partials
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   int s = 0;
   for (; s + 4 <= n; s += 4) {
-    const float4 o0 = *reinterpret_cast<const float4*>(op + static_cast<int64_t>(s) * D);
-    const float4 o1 = *reinterpret_cast<const float4*>(op + static_cast<int64_t>(s + 1) * D);
-    const float4 o2 = *reinterpret_cast<const float4*>(op + static_cast<int64_t>(s + 2) * D);
-    const float4 o3 = *reinterpret_cast<const float4*>(op + static_cast<int64_t>(s + 3) * D);
+    const float4 o0 = *reinterpret_cast<const float4*>(op + s * ostep);
+    const float4 o1 = *reinterpret_cast<const float4*>(op + (s + 1) * ostep);
+    const float4 o2 = *reinterpret_cast<const float4*>(op + (s + 2) * ostep);
+    const float4 o3 = *reinterpret_cast<const float4*>(op + (s + 3) * ostep);
     const float w0 = w[s], w1 = w[s + 1], w2 = w[s + 2], w3 = w[s + 3];
     acc.x = fmaf(w0, o0.x, fmaf(w1, o1.x, fmaf(w2, o2.x, fmaf(w3, o3.x, acc.x))));
     acc.y = fmaf(w0, o0.y, fmaf(w1, o1.y, fmaf(w2, o2.y, fmaf(w3, o3.y, acc.y))));
@@ -235,7 +251,7 @@ __global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
     acc.w = fmaf(w0, o0.w, fmaf(w1, o1.w, fmaf(w2, o2.w, fmaf(w3, o3.w, acc.w))));
   }
   for (; s < n; ++s) {
-    const float4 o = *reinterpret_cast<const float4*>(op + static_cast<int64_t>(s) * D);
+    const float4 o = *reinterpret_cast<const float4*>(op + s * ostep);
     const float ws = w[s];
     acc.x = fmaf(ws, o.x, acc.x);
     acc.y = fmaf(ws, o.y, acc.y);

@@ -106,6 +106,10 @@ DecodeArgs make_decode_args(const DecodeShape& s, const void* q, const void* kc,
   a.num_splits = s.S;
   a.chunk = chunk_pages(page_span_max(s.mbs, s.bs, s.W), s.S);
   a.sliding_window = s.W;
+  a.plan_cta = nullptr;
+  a.plan_pieces = nullptr;
+  a.plan_num_ctas = 0;
+  a.plan_num_pieces = 0;
   a.scale_log2 = scale * kLog2e;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
@@ -127,6 +131,8 @@ CombineArgs make_combine_args(int B, int Hq, int D, int bs, int mbs, int S, int 
   c.chunk = chunk_pages(page_span_max(mbs, bs, W), S);
   c.sliding_window = W;
   c.skip_direct = 0;
+  c.plan_seg = nullptr;
+  c.num_kv_heads = 0;
   return c;
 }
 
@@ -157,7 +163,8 @@ int plan_splits(int B, int Hkv, int mbs, int bs, int W, int num_sms, int ctas_pe
 // makespan wins (ties: fewer splits).
 constexpr double kCtaOverheadBytes = 40.0 * 1024.0;
 int plan_splits_lengths(const int32_t* lens, int B, int Hkv, int Hq, int mbs, int bs, int W,
-                        int D, int kv_dtype, int num_sms, int ctas_per_sm) {
+                        int D, int kv_dtype, int num_sms, int ctas_per_sm,
+                        double* best_estimate = nullptr) {
   const int span = page_span_max(mbs, bs, W);
   const int64_t slots = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * ctas_per_sm;
   const double phb = page_head_bytes(bs, D, kv_dtype);
@@ -207,7 +214,151 @@ int plan_splits_lengths(const int32_t* lens, int B, int Hkv, int Hq, int mbs, in
       best_S = S;
     }
   }
+  if (best_estimate) *best_estimate = best_t;
   return best_S;
+}
+
+// ---------------------------------------------------------------------------
+// Balanced plan. Layout, in int32 words from a 16-byte aligned base:
+//   [0..8)                       header: magic, num_ctas, num_pieces, num_seqs,
+//                                num_kv_heads, block_size, sliding_window,
+//                                max_blocks_per_seq
+//   [8, 8 + num_ctas + 1)        cta_begin: CTA c owns pieces [cta_begin[c], cta_begin[c+1])
+//   [pieces_off, +4*num_pieces)  pieces: (sequence * Hkv + kv head, first key,
+//                                end key, flags; bit 0: the only piece of its head)
+//   [seg_off, +2*B*Hkv)          per (sequence, kv head): first piece, piece count
+constexpr int32_t kPlanMagic = 0x50444231;  // "PDB1"
+constexpr int kMaxBalancedCtas = 1024;      // also bounds the pieces of one head (combine)
+struct PlanLayout {
+  int64_t cta_off, pieces_off, seg_off, words;
+};
+PlanLayout plan_layout(int64_t num_ctas, int64_t num_pieces, int64_t segs) {
+  PlanLayout l;
+  l.cta_off = 8;
+  l.pieces_off = (l.cta_off + num_ctas + 1 + 3) / 4 * 4;
+  l.seg_off = l.pieces_off + 4 * num_pieces;
+  l.words = l.seg_off + 2 * segs;
+  return l;
+}
+int64_t balanced_max_ctas(int num_sms) {
+  const int64_t n = static_cast<int64_t>(num_sms) * 4;  // at most 4 resident CTAs per SM
+  return n < kMaxBalancedCtas ? n : kMaxBalancedCtas;
+}
+size_t balanced_ws_bytes(int64_t num_pieces, int G, int D) {
+  const size_t o = (static_cast<size_t>(num_pieces) * G * D * sizeof(float) + 255) / 256 * 256;
+  const size_t ml = (static_cast<size_t>(num_pieces) * G * 2 * sizeof(float) + 255) / 256 * 256;
+  return o + ml;
+}
+
+// Cut the line of (sequence, kv head) key-page ranges, laid end to end in
+// sequence-major order, into num_ctas equal shares (page granularity); every
+// share that crosses a range boundary becomes several pieces.
+int build_balanced_plan(const int32_t* lens, int B, int Hq, int Hkv, int D, int bs, int mbs,
+                        int W, int kv_dtype, int num_sms, int32_t* plan, size_t plan_bytes,
+                        int32_t* out_ctas, int32_t* out_pieces, size_t* out_ws) {
+  const int G = Hq / Hkv;
+  const int cap = mbs * bs;
+  std::vector<int> L(B), P(B);
+  int64_t T = 0;
+  for (int b = 0; b < B; ++b) {
+    L[b] = lens[b] < 0 ? 0 : (lens[b] > cap ? cap : lens[b]);
+    P[b] = num_key_pages(L[b], W, bs);
+    T += static_cast<int64_t>(P[b]) * Hkv;
+  }
+  int64_t NC = static_cast<int64_t>(num_sms) * balanced_ctas_per_sm(kv_dtype, D, G);
+  if (NC > kMaxBalancedCtas) NC = kMaxBalancedCtas;
+  if (NC > T) NC = T;
+  const int64_t segs = static_cast<int64_t>(B) * Hkv;
+  // pieces: one per range, plus one per share boundary strictly inside a range
+  std::vector<int32_t> pieces;
+  std::vector<int32_t> cta_begin(NC + 1, 0);
+  std::vector<int32_t> seg(2 * segs, 0);
+  pieces.reserve(4 * (segs + NC));
+  auto bound = [&](int64_t c) { return NC > 0 ? c * T / NC : 0; };  // share c starts here
+  int64_t pos = 0;  // line position of the current range's first page
+  int64_t c = 0;    // share holding `pos`
+  int64_t np = 0;
+  for (int b = 0; b < B; ++b) {
+    const int lo = window_lo(L[b], W);
+    const int page0 = lo / bs;  // the sequence's first key page
+    for (int g = 0; g < Hkv; ++g) {
+      const int64_t sid = static_cast<int64_t>(b) * Hkv + g;
+      seg[2 * sid] = static_cast<int32_t>(np);
+      if (P[b] == 0) continue;
+      int64_t a = 0;  // pages of this range already cut
+      while (a < P[b]) {
+        while (c + 1 < NC && bound(c + 1) <= pos + a) {
+          ++c;
+          cta_begin[c] = static_cast<int32_t>(np);
+        }
+        const int64_t e = std::min<int64_t>(P[b], (c + 1 < NC ? bound(c + 1) : T) - pos);
+        const int t_begin = std::max(lo, static_cast<int>((page0 + a) * bs));
+        const int t_end = std::min(L[b], static_cast<int>((page0 + e) * bs));
+        pieces.push_back(static_cast<int32_t>(sid));
+        pieces.push_back(t_begin);
+        pieces.push_back(t_end);
+        pieces.push_back(0);
+        ++np;
+        a = e;
+      }
+      const int32_t count = static_cast<int32_t>(np) - seg[2 * sid];
+      seg[2 * sid + 1] = count;
+      if (count == 1) pieces[4 * (np - 1) + 3] = 1;  // its head's only piece: write out
+      pos += P[b];
+    }
+  }
+  for (int64_t k = c + 1; k <= NC; ++k) cta_begin[k] = static_cast<int32_t>(np);
+  const PlanLayout lay = plan_layout(NC, np, segs);
+  if (plan_bytes < static_cast<size_t>(lay.words) * 4) return PD_ERR_WORKSPACE_TOO_SMALL;
+  plan[0] = kPlanMagic;
+  plan[1] = static_cast<int32_t>(NC);
+  plan[2] = static_cast<int32_t>(np);
+  plan[3] = B;
+  plan[4] = Hkv;
+  plan[5] = bs;
+  plan[6] = W;
+  plan[7] = mbs;
+  for (int64_t k = 0; k <= NC; ++k) plan[lay.cta_off + k] = cta_begin[k];
+  for (int64_t k = lay.cta_off + NC + 1; k < lay.pieces_off; ++k) plan[k] = 0;
+  std::copy(pieces.begin(), pieces.end(), plan + lay.pieces_off);
+  std::copy(seg.begin(), seg.end(), plan + lay.seg_off);
+  *out_ctas = static_cast<int32_t>(NC);
+  *out_pieces = static_cast<int32_t>(np);
+  *out_ws = balanced_ws_bytes(np, G, D);
+  return PD_OK;
+}
+
+// Balanced schedule vs split schedule, both in the split planner's units
+// (bytes one CTA slot streams): the balanced kernel gives every CTA the same
+// pages, at a per-tile premium (its piece bookkeeping), one CTA start-up
+// like any CTA, and a switch-over cost per extra piece; the split schedule's
+// estimate is the planner's best makespan. The premiums, 8 % (head_dim <=
+// 128) and 12 % (head_dim 256 / 512, whose consumer warps also meet at a
+// barrier every tile), are the ones that order the bench workloads as
+// measured (equal lengths: split; unequal: balanced).
+constexpr double kBalancedTilePremium = 1.08;
+constexpr double kBalancedTilePremiumSplitD = 1.12;
+constexpr double kPieceOverheadBytes = 8.0 * 1024.0;
+int prefer_balanced(const int32_t* lens, int B, int Hq, int Hkv, int mbs, int bs, int W, int D,
+                    int kv_dtype, int num_sms) {
+  double split_t = 0.0;
+  plan_splits_lengths(lens, B, Hkv, Hq, mbs, bs, W, D, kv_dtype, num_sms,
+                      mma_ctas_per_sm_estimate(kv_dtype, D), &split_t);
+  const int cap = mbs * bs;
+  int64_t T = 0;
+  for (int b = 0; b < B; ++b) {
+    const int L = lens[b] < 0 ? 0 : (lens[b] > cap ? cap : lens[b]);
+    T += static_cast<int64_t>(num_key_pages(L, W, bs)) * Hkv;
+  }
+  if (T == 0) return 0;
+  int64_t NC = static_cast<int64_t>(num_sms) * balanced_ctas_per_sm(kv_dtype, D, Hq / Hkv);
+  if (NC > kMaxBalancedCtas) NC = kMaxBalancedCtas;
+  if (NC > T) NC = T;
+  const double pieces_per_cta = static_cast<double>(static_cast<int64_t>(B) * Hkv + NC) / NC;
+  const double premium = D <= 128 ? kBalancedTilePremium : kBalancedTilePremiumSplitD;
+  const double bal_t = premium * T * page_head_bytes(bs, D, kv_dtype) / NC +
+                       kCtaOverheadBytes + (pieces_per_cta - 1.0) * kPieceOverheadBytes;
+  return bal_t < split_t ? 1 : 0;
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? PD_OK : PD_ERR_CUDA; }
@@ -418,6 +569,153 @@ int pd_decode(const void* q, const void* k_cache, const void* v_cache, const int
                                     out);
   c.skip_direct = 1;
   return cuda_status(launch_decode_combine(c, head_dim, st));
+}
+
+int pd_prefer_balanced(const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t max_blocks_per_seq, int32_t block_size,
+                       int32_t sliding_window, int32_t head_dim, int32_t kv_dtype,
+                       int32_t num_sms) {
+  if (num_seqs < 0 || (num_seqs > 0 && seq_lens == nullptr) || num_kv_heads <= 0 ||
+      num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 || max_blocks_per_seq <= 0 ||
+      block_size <= 0 || sliding_window < 0 || num_sms <= 0 || !head_dim_ok(head_dim) ||
+      !dtype_ok(kv_dtype) || num_q_heads / num_kv_heads > kMaxGroup)
+    return -PD_ERR_INVALID_ARG;
+  if (num_seqs == 0) return 0;
+  return prefer_balanced(seq_lens, num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq,
+                         block_size, sliding_window, head_dim, kv_dtype, num_sms);
+}
+
+size_t pd_balanced_plan_bytes(int32_t num_seqs, int32_t num_kv_heads, int32_t num_sms) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || num_sms <= 0) return 0;
+  const int64_t nc = balanced_max_ctas(num_sms);
+  const int64_t segs = static_cast<int64_t>(num_seqs) * num_kv_heads;
+  return static_cast<size_t>(plan_layout(nc, segs + nc, segs).words) * 4;
+}
+
+int pd_balanced_plan(const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                     int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                     int32_t max_blocks_per_seq, int32_t sliding_window, int32_t kv_dtype,
+                     int32_t num_sms, void* plan, size_t plan_bytes, int32_t* num_ctas,
+                     int32_t* num_pieces, size_t* workspace_bytes) {
+  if (num_seqs < 0 || num_seqs > 65535 || (num_seqs > 0 && seq_lens == nullptr) ||
+      num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
+      max_blocks_per_seq <= 0 || sliding_window < 0 || num_sms <= 0 || plan == nullptr ||
+      (reinterpret_cast<uintptr_t>(plan) & 15u) || num_ctas == nullptr ||
+      num_pieces == nullptr || workspace_bytes == nullptr)
+    return PD_ERR_INVALID_ARG;
+  if (num_q_heads / num_kv_heads > kMaxGroup) return PD_ERR_UNSUPPORTED;
+  if (!head_dim_ok(head_dim) || !block_size_ok(block_size) || !dtype_ok(kv_dtype))
+    return PD_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(max_blocks_per_seq) * block_size > (int64_t{1} << 30))
+    return PD_ERR_INVALID_ARG;
+  return build_balanced_plan(seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                             max_blocks_per_seq, sliding_window, kv_dtype, num_sms,
+                             static_cast<int32_t*>(plan), plan_bytes, num_ctas, num_pieces,
+                             workspace_bytes);
+}
+
+}  // extern "C"
+
+namespace {
+// pd_decode_balanced and its two halves: which of the two kernels to launch.
+int decode_balanced(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, const void* plan, size_t plan_bytes, void* out,
+                    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                    int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
+                    int64_t num_blocks, float scale, int32_t sliding_window, int32_t kv_dtype,
+                    float k_scale, float v_scale, int32_t num_ctas, int32_t num_pieces,
+                    void* workspace, size_t workspace_bytes, void* stream, bool partial,
+                    bool combine) {
+  // shape checks shared with pd_decode (S = 1 stands for the split count)
+  const DecodeShape sh{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       max_blocks_per_seq, 1, sliding_window, kv_dtype, num_blocks};
+  if (num_ctas < 0 || num_ctas > kMaxBalancedCtas || num_pieces < 0 ||
+      (num_ctas == 0) != (num_pieces == 0))
+    return PD_ERR_INVALID_ARG;
+  const int64_t segs = static_cast<int64_t>(num_seqs) * (num_kv_heads > 0 ? num_kv_heads : 0);
+  if (static_cast<int64_t>(num_pieces) > segs + num_ctas) return PD_ERR_INVALID_ARG;
+  int rc = check_decode(sh, q, k_cache, v_cache, block_tables, block_tables, k_scale, v_scale,
+                        workspace, SIZE_MAX);
+  if (rc != PD_OK || num_seqs == 0) return rc;
+  if (!isfinite(scale) || !dev_ptr_ok(out) || !dev_ptr_ok(plan)) return PD_ERR_INVALID_ARG;
+  const PlanLayout lay = plan_layout(num_ctas, num_pieces, segs);
+  if (plan_bytes < static_cast<size_t>(lay.words) * 4) return PD_ERR_INVALID_ARG;
+  const int G = num_q_heads / num_kv_heads;
+  if (workspace_bytes < balanced_ws_bytes(num_pieces, G, head_dim))
+    return PD_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo* dev = nullptr;
+  if (current_device(&dev) != cudaSuccess) return PD_ERR_CUDA;
+  const int32_t* pl = static_cast<const int32_t*>(plan);
+  DecodeArgs a = make_decode_args(sh, q, k_cache, v_cache, block_tables, nullptr, scale, k_scale,
+                                  v_scale, workspace, dev->flags);
+  // balanced workspace: O [pieces][G][D], then (m, l) [pieces][G]
+  a.ws_o = static_cast<float*>(workspace);
+  a.ws_ml = reinterpret_cast<float2*>(
+      static_cast<char*>(workspace) +
+      (static_cast<size_t>(num_pieces) * G * head_dim * sizeof(float) + 255) / 256 * 256);
+  a.out = static_cast<uint16_t*>(out);
+  a.direct = 1;
+  a.plan_cta = pl + lay.cta_off;
+  a.plan_pieces = reinterpret_cast<const int4*>(pl + lay.pieces_off);
+  a.plan_num_ctas = num_ctas;
+  a.plan_num_pieces = num_pieces;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (partial && launch_decode_partial_balanced(a, head_dim, kv_dtype, st) != cudaSuccess)
+    return PD_ERR_CUDA;
+  if (!combine) return PD_OK;
+  CombineArgs c = make_combine_args(num_seqs, num_q_heads, head_dim, block_size,
+                                    max_blocks_per_seq, 1, sliding_window, workspace, nullptr,
+                                    out);
+  c.ws_o = a.ws_o;
+  c.ws_ml = a.ws_ml;
+  c.plan_seg = pl + lay.seg_off;
+  c.num_kv_heads = num_kv_heads;
+  return cuda_status(launch_decode_combine(c, head_dim, st));
+}
+}  // namespace
+
+extern "C" {
+
+int pd_decode_balanced(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const void* plan, size_t plan_bytes,
+                       void* out, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
+                       int64_t num_blocks, float scale, int32_t sliding_window,
+                       int32_t kv_dtype, float k_scale, float v_scale, int32_t num_ctas,
+                       int32_t num_pieces, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  return decode_balanced(q, k_cache, v_cache, block_tables, plan, plan_bytes, out, num_seqs,
+                         num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                         num_blocks, scale, sliding_window, kv_dtype, k_scale, v_scale, num_ctas,
+                         num_pieces, workspace, workspace_bytes, stream, true, true);
+}
+
+int pd_decode_balanced_partial(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const void* plan, size_t plan_bytes,
+                               void* out, int32_t num_seqs, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
+                               int32_t sliding_window, int32_t kv_dtype, float k_scale,
+                               float v_scale, int32_t num_ctas, int32_t num_pieces,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_balanced(q, k_cache, v_cache, block_tables, plan, plan_bytes, out, num_seqs,
+                         num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                         num_blocks, scale, sliding_window, kv_dtype, k_scale, v_scale, num_ctas,
+                         num_pieces, workspace, workspace_bytes, stream, true, false);
+}
+
+int pd_decode_balanced_combine(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const void* plan, size_t plan_bytes,
+                               void* out, int32_t num_seqs, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
+                               int32_t sliding_window, int32_t kv_dtype, float k_scale,
+                               float v_scale, int32_t num_ctas, int32_t num_pieces,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_balanced(q, k_cache, v_cache, block_tables, plan, plan_bytes, out, num_seqs,
+                         num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                         num_blocks, scale, sliding_window, kv_dtype, k_scale, v_scale, num_ctas,
+                         num_pieces, workspace, workspace_bytes, stream, false, true);
 }
 
 int pd_device_status(int32_t* flags, int32_t reset) {

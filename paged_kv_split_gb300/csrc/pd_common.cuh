@@ -152,6 +152,11 @@ struct DecodeArgs {
   int64_t data_bytes;            // NVFP4 data-section bytes
   int num_seqs, num_q_heads, num_kv_heads, group, block_size, max_blocks_per_seq;
   int num_splits, chunk, sliding_window;
+  // balanced plan (pd_decode_balanced only): per-CTA piece ranges and the
+  // pieces (sequence * Hkv + kv head, first key, end key, flags)
+  const int32_t* plan_cta;
+  const int4* plan_pieces;
+  int plan_num_ctas, plan_num_pieces;
   float scale_log2;              // scale * log2(e)
   float k_scale, v_scale;
 };
@@ -163,6 +168,11 @@ struct CombineArgs {
   uint16_t* out;
   int num_seqs, num_q_heads, block_size, max_blocks_per_seq, num_splits, chunk, sliding_window;
   int skip_direct;               // 1: sequences with one key-holding split are already written
+  // balanced plan: per (sequence, kv head) its first piece and piece count;
+  // when set, the partials of q head h are pieces first.. of its kv head
+  // (row piece * group + h % group) instead of the S splits
+  const int32_t* plan_seg;
+  int num_kv_heads;
 };
 
 // Sequence length as the kernels use it: clamped to the block table, with a
@@ -195,5 +205,9 @@ cudaError_t launch_decode_partial_mma(const DecodeArgs& a, int head_dim, int kv_
 // Resident CTAs per SM of the tensor-core partial kernel, from its shared
 // memory per CTA (host-only estimate; no CUDA call).
 int mma_ctas_per_sm_estimate(int kv_dtype, int head_dim);
+cudaError_t launch_decode_partial_balanced(const DecodeArgs& a, int head_dim, int kv_dtype,
+                                           cudaStream_t st);
+// Resident CTAs per SM of the balanced partial kernel for a GQA group size.
+int balanced_ctas_per_sm(int kv_dtype, int head_dim, int group);
 cudaError_t launch_decode_combine(const CombineArgs& a, int head_dim, cudaStream_t st);
 }  // namespace pd
