@@ -1020,7 +1020,11 @@ bool encode_cache_map(CUtensorMap* m, const void* base, int kv_dtype, int D, int
       m, esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
       const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
       swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+      // L2 fills no wider than one head's row: a wider fill would pull in the
+      // next head's bytes, which another CTA reads at some other time
+      D * esz >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                     : (D * esz >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                       : CU_TENSOR_MAP_L2_PROMOTION_L2_64B),
       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return rc == CUDA_SUCCESS;
 }
