@@ -306,6 +306,10 @@ __global__ void __launch_bounds__(kMmaThreads)
   // let the dependent combine grid be scheduled as this grid drains (it waits
   // for this grid's completion before reading the workspace)
   asm volatile("griddepcontrol.launch_dependents;");
+  // Launched as a programmatic dependent of whatever came before on the
+  // stream (the previous step's combine, say): nothing global is read or
+  // written before that grid has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int g = blockIdx.x;  // kv head
   const int s = blockIdx.y;  // split
   const int b = blockIdx.z;  // sequence
@@ -470,7 +474,7 @@ __global__ void __launch_bounds__(kMmaThreads)
   uint32_t qf[C::kKSteps][NT][2];
   float qmul[NT][2];  // score multiplier (log2 units) of the two head columns of this thread
   {
-    const uint16_t* qb = a.q + (static_cast<int64_t>(b) * a.num_q_heads + g * G) * D;
+    const uint16_t* qb = a.q + static_cast<int64_t>(b) * a.q_stride + g * G * D;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int n = nt * 8 + r;  // q head row of the B fragment
@@ -1054,8 +1058,18 @@ cudaError_t launch_mma_cfg(const DecodeArgs& a, cudaStream_t st) {
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const dim3 grid(a.num_kv_heads, a.num_splits, a.num_seqs);
-  kern<<<grid, kMmaThreads, C::kSmemBytes, st>>>(tk, tv, a);
-  return cudaGetLastError();
+  // a programmatic dependent of the previous work on the stream
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kMmaThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, a);
 }
 
 template <int FMT, int D, int NT>

@@ -46,6 +46,10 @@ template <int FMT, int D>
 __global__ void __launch_bounds__(kThreads) partial_simple_kernel(const DecodeArgs a) {
   // let the dependent combine grid be scheduled as this grid drains
   asm volatile("griddepcontrol.launch_dependents;");
+  // Launched as a programmatic dependent of whatever came before on the
+  // stream (the previous step's combine, say): nothing global is read or
+  // written before that grid has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int kPerLane = D / 32;
   constexpr int kAccMax = kMaxGroup * D / kThreads;
   const int g = blockIdx.x;  // kv head
@@ -69,7 +73,7 @@ __global__ void __launch_bounds__(kThreads) partial_simple_kernel(const DecodeAr
   float* l_s = m_s + kMaxGroup;     // [G] running sum
   float* alpha_s = l_s + kMaxGroup; // [G] rescale factor of the current tile
 
-  const uint16_t* qg = a.q + (static_cast<int64_t>(b) * a.num_q_heads + g * G) * D;
+  const uint16_t* qg = a.q + static_cast<int64_t>(b) * a.q_stride + g * G * D;
   for (int i = threadIdx.x; i < G * D; i += kThreads) qs[i] = bf16_to_f32(qg[i]) * a.scale_log2;
   if (threadIdx.x < G) {
     m_s[threadIdx.x] = -INFINITY;
@@ -172,6 +176,8 @@ __global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
   // Launched as a programmatic dependent of the partial kernel: wait until
   // that grid has completed and its workspace writes are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // and let the next step's partial kernel be scheduled as this grid drains
+  asm volatile("griddepcontrol.launch_dependents;");
   constexpr int kThreads = D / 4;
   const int h = blockIdx.x;
   const int b = blockIdx.y;
@@ -278,8 +284,18 @@ cudaError_t launch_simple(const DecodeArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   const dim3 grid(a.num_kv_heads, a.num_splits, a.num_seqs);
-  kern<<<grid, kThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  // a programmatic dependent of the previous work on the stream
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 template <int FMT>

@@ -85,6 +85,7 @@ DecodeArgs make_decode_args(const DecodeShape& s, const void* q, const void* kc,
                             float v_scale, void* ws, int* flags) {
   DecodeArgs a;
   a.q = static_cast<const uint16_t*>(q);
+  a.q_stride = static_cast<int64_t>(s.Hq) * s.D;
   a.k_cache = static_cast<const uint8_t*>(kc);
   a.v_cache = static_cast<const uint8_t*>(vc);
   a.block_tables = bt;
@@ -363,6 +364,13 @@ int prefer_balanced(const int32_t* lens, int B, int Hq, int Hkv, int mbs, int bs
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? PD_OK : PD_ERR_CUDA; }
 
+// A q row stride (elements between consecutive sequences' q rows): 0 means
+// packed (Hq * D); otherwise at least Hq * D and a multiple of 8 elements so
+// that every row starts on a 16-byte boundary.
+bool q_stride_ok(int64_t q_stride, int Hq, int D) {
+  return q_stride == 0 || (q_stride >= static_cast<int64_t>(Hq) * D && q_stride % 8 == 0);
+}
+
 // The tensor-core partial kernel runs by default; PD_PARTIAL_KERNEL=simple
 // selects the CUDA-core kernel instead (kept as an independent cross-check).
 bool use_simple_partial() {
@@ -480,13 +488,15 @@ int pd_absmax_bf16(const void* data, int64_t n, float* out_max, void* stream) {
                                    static_cast<cudaStream_t>(stream)));
 }
 
-int pd_decode_partial(const void* q, const void* k_cache, const void* v_cache,
-                      const int32_t* block_tables, const int32_t* seq_lens, int32_t num_seqs,
-                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                      int32_t block_size, int32_t max_blocks_per_seq, int64_t num_blocks,
-                      float scale, int32_t num_splits, int32_t sliding_window, int32_t kv_dtype,
-                      float k_scale, float v_scale, void* workspace, size_t workspace_bytes,
-                      void* stream) {
+}  // extern "C"
+
+namespace {
+int partial_impl(const void* q, const void* k_cache, const void* v_cache,
+                 const int32_t* block_tables, const int32_t* seq_lens, int32_t num_seqs,
+                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                 int32_t max_blocks_per_seq, int64_t num_blocks, float scale, int32_t num_splits,
+                 int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
+                 void* workspace, size_t workspace_bytes, void* stream, int64_t q_stride) {
   const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                       max_blocks_per_seq, num_splits, sliding_window, kv_dtype, num_blocks};
   const int rc = check_decode(s, q, k_cache, v_cache, block_tables, seq_lens, k_scale, v_scale,
@@ -495,11 +505,29 @@ int pd_decode_partial(const void* q, const void* k_cache, const void* v_cache,
   if (!isfinite(scale)) return PD_ERR_INVALID_ARG;
   DeviceInfo* dev = nullptr;
   if (current_device(&dev) != cudaSuccess) return PD_ERR_CUDA;
-  const DecodeArgs a = make_decode_args(s, q, k_cache, v_cache, block_tables, seq_lens, scale,
-                                        k_scale, v_scale, workspace, dev->flags);
+  DecodeArgs a = make_decode_args(s, q, k_cache, v_cache, block_tables, seq_lens, scale, k_scale,
+                                  v_scale, workspace, dev->flags);
+  if (!q_stride_ok(q_stride, num_q_heads, head_dim)) return PD_ERR_INVALID_ARG;
+  if (q_stride) a.q_stride = q_stride;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   return cuda_status(use_simple_partial() ? launch_decode_partial(a, head_dim, kv_dtype, st)
                                           : launch_decode_partial_mma(a, head_dim, kv_dtype, st));
+}
+}  // namespace
+
+extern "C" {
+
+int pd_decode_partial(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* seq_lens, int32_t num_seqs,
+                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, int32_t max_blocks_per_seq, int64_t num_blocks,
+                      float scale, int32_t num_splits, int32_t sliding_window, int32_t kv_dtype,
+                      float k_scale, float v_scale, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  return partial_impl(q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_q_heads,
+                      num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
+                      num_splits, sliding_window, kv_dtype, k_scale, v_scale, workspace,
+                      workspace_bytes, stream, 0);
 }
 
 int pd_decode_combine(const void* workspace, size_t workspace_bytes, const int32_t* seq_lens,
@@ -521,12 +549,17 @@ int pd_decode_combine(const void* workspace, size_t workspace_bytes, const int32
   return cuda_status(launch_decode_combine(c, head_dim, static_cast<cudaStream_t>(stream)));
 }
 
-int pd_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
-              const int32_t* seq_lens, void* out, int32_t num_seqs, int32_t num_q_heads,
-              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-              int32_t max_blocks_per_seq, int64_t num_blocks, float scale, int32_t num_splits,
-              int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
-              void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+int decode_split(const void* q, const void* k_cache, const void* v_cache,
+                 const int32_t* block_tables, const int32_t* seq_lens, void* out,
+                 int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                 int32_t block_size, int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
+                 int32_t num_splits, int32_t sliding_window, int32_t kv_dtype, float k_scale,
+                 float v_scale, void* workspace, size_t workspace_bytes, void* stream,
+                 int64_t q_stride) {
+  if (!q_stride_ok(q_stride, num_q_heads, head_dim)) return PD_ERR_INVALID_ARG;
   if (num_splits < 0 || num_splits > kMaxSplits) return PD_ERR_INVALID_ARG;
   if (num_seqs > 0 && !dev_ptr_ok(out)) return PD_ERR_INVALID_ARG;
   int S = num_splits;
@@ -540,10 +573,10 @@ int pd_decode(const void* q, const void* k_cache, const void* v_cache, const int
                     dev->num_sms, mma_ctas_per_sm_estimate(kv_dtype, head_dim));
   }
   if (use_simple_partial()) {
-    int rc = pd_decode_partial(q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
-                               num_q_heads, num_kv_heads, head_dim, block_size,
-                               max_blocks_per_seq, num_blocks, scale, S, sliding_window, kv_dtype,
-                               k_scale, v_scale, workspace, workspace_bytes, stream);
+    int rc = partial_impl(q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_q_heads,
+                          num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+                          scale, S, sliding_window, kv_dtype, k_scale, v_scale, workspace,
+                          workspace_bytes, stream, q_stride);
     if (rc != PD_OK || num_seqs == 0) return rc;
     return pd_decode_combine(workspace, workspace_bytes, seq_lens, out, num_seqs, num_q_heads,
                              head_dim, block_size, max_blocks_per_seq, S, sliding_window, stream);
@@ -562,6 +595,7 @@ int pd_decode(const void* q, const void* k_cache, const void* v_cache, const int
                                   v_scale, workspace, dev->flags);
   a.out = static_cast<uint16_t*>(out);
   a.direct = 1;
+  if (q_stride) a.q_stride = q_stride;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_decode_partial_mma(a, head_dim, kv_dtype, st) != cudaSuccess) return PD_ERR_CUDA;
   CombineArgs c = make_combine_args(num_seqs, num_q_heads, head_dim, block_size,
@@ -569,6 +603,35 @@ int pd_decode(const void* q, const void* k_cache, const void* v_cache, const int
                                     out);
   c.skip_direct = 1;
   return cuda_status(launch_decode_combine(c, head_dim, st));
+}
+}  // namespace
+
+extern "C" {
+
+int pd_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+              const int32_t* seq_lens, void* out, int32_t num_seqs, int32_t num_q_heads,
+              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+              int32_t max_blocks_per_seq, int64_t num_blocks, float scale, int32_t num_splits,
+              int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
+              void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_split(q, k_cache, v_cache, block_tables, seq_lens, out, num_seqs, num_q_heads,
+                      num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
+                      num_splits, sliding_window, kv_dtype, k_scale, v_scale, workspace,
+                      workspace_bytes, stream, 0);
+}
+
+int pd_decode_strided(const void* q, int64_t q_stride, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* seq_lens, void* out,
+                      int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
+                      int64_t num_blocks, float scale, int32_t num_splits, int32_t sliding_window,
+                      int32_t kv_dtype, float k_scale, float v_scale, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (q_stride <= 0) return PD_ERR_INVALID_ARG;
+  return decode_split(q, k_cache, v_cache, block_tables, seq_lens, out, num_seqs, num_q_heads,
+                      num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
+                      num_splits, sliding_window, kv_dtype, k_scale, v_scale, workspace,
+                      workspace_bytes, stream, q_stride);
 }
 
 int pd_prefer_balanced(const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
@@ -625,7 +688,8 @@ int decode_balanced(const void* q, const void* k_cache, const void* v_cache,
                     int64_t num_blocks, float scale, int32_t sliding_window, int32_t kv_dtype,
                     float k_scale, float v_scale, int32_t num_ctas, int32_t num_pieces,
                     void* workspace, size_t workspace_bytes, void* stream, bool partial,
-                    bool combine) {
+                    bool combine, int64_t q_stride = 0) {
+  if (!q_stride_ok(q_stride, num_q_heads, head_dim)) return PD_ERR_INVALID_ARG;
   // shape checks shared with pd_decode (S = 1 stands for the split count)
   const DecodeShape sh{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                        max_blocks_per_seq, 1, sliding_window, kv_dtype, num_blocks};
@@ -659,6 +723,7 @@ int decode_balanced(const void* q, const void* k_cache, const void* v_cache,
   a.plan_pieces = reinterpret_cast<const int4*>(pl + lay.pieces_off);
   a.plan_num_ctas = num_ctas;
   a.plan_num_pieces = num_pieces;
+  if (q_stride) a.q_stride = q_stride;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (partial && launch_decode_partial_balanced(a, head_dim, kv_dtype, st) != cudaSuccess)
     return PD_ERR_CUDA;
@@ -688,6 +753,22 @@ int pd_decode_balanced(const void* q, const void* k_cache, const void* v_cache,
                          num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                          num_blocks, scale, sliding_window, kv_dtype, k_scale, v_scale, num_ctas,
                          num_pieces, workspace, workspace_bytes, stream, true, true);
+}
+
+int pd_decode_balanced_strided(const void* q, int64_t q_stride, const void* k_cache,
+                               const void* v_cache, const int32_t* block_tables,
+                               const void* plan, size_t plan_bytes, void* out, int32_t num_seqs,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t block_size, int32_t max_blocks_per_seq,
+                               int64_t num_blocks, float scale, int32_t sliding_window,
+                               int32_t kv_dtype, float k_scale, float v_scale, int32_t num_ctas,
+                               int32_t num_pieces, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  if (q_stride <= 0) return PD_ERR_INVALID_ARG;
+  return decode_balanced(q, k_cache, v_cache, block_tables, plan, plan_bytes, out, num_seqs,
+                         num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                         num_blocks, scale, sliding_window, kv_dtype, k_scale, v_scale, num_ctas,
+                         num_pieces, workspace, workspace_bytes, stream, true, true, q_stride);
 }
 
 int pd_decode_balanced_partial(const void* q, const void* k_cache, const void* v_cache,

@@ -135,7 +135,8 @@ __host__ __device__ __forceinline__ size_t ws_total_bytes(int B, int Hq, int D, 
 // ---------------------------------------------------------------------------
 // Kernel argument blocks.
 struct DecodeArgs {
-  const uint16_t* q;             // [B][Hq][D] bf16
+  const uint16_t* q;             // [B][Hq][D] bf16, sequence b's rows at b * q_stride
+  int64_t q_stride;              // elements between consecutive sequences' q rows
   const uint8_t* k_cache;
   const uint8_t* v_cache;
   const int32_t* block_tables;   // [B][MBS]
