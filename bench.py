@@ -193,24 +193,34 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x: float, world: int) -> float:
+def _reduce_over_ranks(x: float, world: int, op) -> float:
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    # the reduction's tensor lives where the process group's backend wants it
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=op)
     return float(t.item())
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    import torch.distributed as dist
+    return _reduce_over_ranks(x, world, dist.ReduceOp.MAX if world > 1 else None)
 
 
 def sum_over_ranks(x: float, world: int) -> float:
-    if world == 1:
-        return x
-    import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return _reduce_over_ranks(x, world, dist.ReduceOp.SUM if world > 1 else None)
+
+
+def job_throughput(ms_step_local: float, bytes_local: float, world: int):
+    """Whole-job figures of a replicas run: the slowest rank's ms per step and
+    the bytes all ranks moved per step, divided (GB/s)."""
+    ms_step = max_over_ranks(ms_step_local, world)
+    total_bytes = sum_over_ranks(bytes_local, world)
+    return ms_step, total_bytes, total_bytes / (ms_step * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------------------
@@ -477,9 +487,7 @@ def run_pd(args, rank, world, local):
     graph_w_us = timed_replays(graphs_w, n_graph)
 
     ms_step_local = total_ms / args.steps
-    ms_step = max_over_ranks(ms_step_local, world)
-    total_bytes = sum_over_ranks(ab["total"], world)
-    value = total_bytes / (ms_step * 1e-3) / 1e9
+    ms_step, total_bytes, value = job_throughput(ms_step_local, ab["total"], world)
 
     # roofline of the dominant kernel (the split-KV partial)
     part_ms = statistics.mean(partial_ms)
