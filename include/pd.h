@@ -185,19 +185,21 @@ int pd_decode(const void* q, const void* k_cache, const void* v_cache, const int
               int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
               void* workspace, size_t workspace_bytes, void* stream);
 
-/* pd_decode with q read from rows that need not be packed, as in a fused QKV
- * buffer ([metrale] `q_stride`; AstrAI "strided Q"): sequence b's q heads
- * are the num_q_heads * head_dim contiguous bf16 values at q + b * q_stride.
- * q_stride is in elements, >= num_q_heads * head_dim and a multiple of 8
- * (16-byte aligned rows); PD_ERR_INVALID_ARG otherwise. Everything else is as
- * pd_decode; the output is packed [num_seqs][num_q_heads][head_dim]. */
+/* pd_decode with q read from and out written to rows that need not be
+ * packed, as in a fused QKV buffer ([metrale] `q_stride`; [AstrAI]
+ * "stride-based addressing for Q/KV/O"): sequence b's q heads are the
+ * num_q_heads * head_dim contiguous bf16 values at q + b * q_stride, and its
+ * output heads go to out + b * out_stride. Both strides are in elements,
+ * >= num_q_heads * head_dim and a multiple of 8 (16-byte aligned rows);
+ * PD_ERR_INVALID_ARG otherwise. Everything else is as pd_decode. */
 int pd_decode_strided(const void* q, int64_t q_stride, const void* k_cache, const void* v_cache,
                       const int32_t* block_tables, const int32_t* seq_lens, void* out,
-                      int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                      int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
-                      int64_t num_blocks, float scale, int32_t num_splits, int32_t sliding_window,
-                      int32_t kv_dtype, float k_scale, float v_scale, void* workspace,
-                      size_t workspace_bytes, void* stream);
+                      int64_t out_stride, int32_t num_seqs, int32_t num_q_heads,
+                      int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                      int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
+                      int32_t num_splits, int32_t sliding_window, int32_t kv_dtype,
+                      float k_scale, float v_scale, void* workspace, size_t workspace_bytes,
+                      void* stream);
 
 /* The first half of pd_decode alone: writes the S partials (O_s normalised,
  * m_s, l_s) of every (sequence, q head) to the workspace ([metrale]: "each
@@ -290,10 +292,11 @@ int pd_decode_balanced(const void* q, const void* k_cache, const void* v_cache,
                        int32_t num_pieces, void* workspace, size_t workspace_bytes,
                        void* stream);
 
-/* pd_decode_balanced with strided q rows (q_stride as for pd_decode_strided). */
+/* pd_decode_balanced with strided q and output rows (as for pd_decode_strided). */
 int pd_decode_balanced_strided(const void* q, int64_t q_stride, const void* k_cache,
                                const void* v_cache, const int32_t* block_tables,
-                               const void* plan, size_t plan_bytes, void* out, int32_t num_seqs,
+                               const void* plan, size_t plan_bytes, void* out,
+                               int64_t out_stride, int32_t num_seqs,
                                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                int32_t block_size, int32_t max_blocks_per_seq,
                                int64_t num_blocks, float scale, int32_t sliding_window,

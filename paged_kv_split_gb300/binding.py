@@ -48,7 +48,7 @@ _lib.pd_absmax_bf16.argtypes, _lib.pd_absmax_bf16.restype = [_P, _i64, _P, _P], 
 _DECODE_ARGS = [_P, _P, _P, _P, _P, _P, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _f32, _i32,
                 _i32, _i32, _f32, _f32, _P, _sz, _P]
 _lib.pd_decode.argtypes, _lib.pd_decode.restype = _DECODE_ARGS, ctypes.c_int
-_lib.pd_decode_strided.argtypes = [_P, _i64] + _DECODE_ARGS[1:]
+_lib.pd_decode_strided.argtypes = [_P, _i64] + _DECODE_ARGS[1:6] + [_i64] + _DECODE_ARGS[6:]
 _lib.pd_decode_strided.restype = ctypes.c_int
 _lib.pd_decode_partial.argtypes = [_P, _P, _P, _P, _P, _i32, _i32, _i32, _i32, _i32, _i32, _i64,
                                    _f32, _i32, _i32, _i32, _f32, _f32, _P, _sz, _P]
@@ -67,7 +67,8 @@ _lib.pd_decode_balanced.argtypes = [_P, _P, _P, _P, _P, _sz, _P, _i32, _i32, _i3
                                     _i32, _i64, _f32, _i32, _i32, _f32, _f32, _i32, _i32, _P,
                                     _sz, _P]
 _lib.pd_decode_balanced.restype = ctypes.c_int
-_lib.pd_decode_balanced_strided.argtypes = [_P, _i64] + _lib.pd_decode_balanced.argtypes[1:]
+_lib.pd_decode_balanced_strided.argtypes = ([_P, _i64] + _lib.pd_decode_balanced.argtypes[1:7] +
+                                            [_i64] + _lib.pd_decode_balanced.argtypes[7:])
 _lib.pd_decode_balanced_strided.restype = ctypes.c_int
 for _fn in ("pd_decode_balanced_partial", "pd_decode_balanced_combine"):
     getattr(_lib, _fn).argtypes = _lib.pd_decode_balanced.argtypes
@@ -382,23 +383,29 @@ def pd_prefer_balanced(seq_lens_host, *, num_q_heads, num_kv_heads, max_blocks_p
 
 
 # ---- strided q (fused QKV buffers) -----------------------------------------
+def _strided_rows(rows, num_q_heads, head_dim, name):
+    """rows: bf16 [B, row] (contiguous), the heads in the first Hq * D of a row."""
+    if rows.dim() != 2 or rows.dtype != torch.bfloat16 or not rows.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bf16 [num_seqs, row] tensor")
+    if rows.shape[1] < num_q_heads * head_dim:
+        raise ValueError(f"a {name} row is shorter than num_q_heads * head_dim")
+    return int(rows.shape[0]), int(rows.shape[1])
+
+
 def _strided_q(q_rows, num_q_heads, head_dim):
-    """q_rows: bf16 [B, row] (contiguous), q heads in the first Hq * D of a row."""
-    if q_rows.dim() != 2 or q_rows.dtype != torch.bfloat16 or not q_rows.is_contiguous():
-        raise ValueError("q_rows must be a contiguous bf16 [num_seqs, row] tensor")
-    if q_rows.shape[1] < num_q_heads * head_dim:
-        raise ValueError("a q row is shorter than num_q_heads * head_dim")
-    return int(q_rows.shape[0]), int(q_rows.shape[1])
+    return _strided_rows(q_rows, num_q_heads, head_dim, "q_rows")
 
 
-def pd_decode_strided(q_rows, k_cache, v_cache, block_tables, seq_lens, out, *, num_q_heads,
-                      head_dim, num_kv_heads, block_size, num_blocks, scale, num_splits=0,
-                      sliding_window=0, kv_dtype=PD_KV_BF16, k_scale=1.0, v_scale=1.0,
-                      workspace=None, stream=None):
-    """pd_decode with sequence b's q heads at q_rows[b, :num_q_heads * head_dim]."""
+def pd_decode_strided(q_rows, k_cache, v_cache, block_tables, seq_lens, out_rows, *,
+                      num_q_heads, head_dim, num_kv_heads, block_size, num_blocks, scale,
+                      num_splits=0, sliding_window=0, kv_dtype=PD_KV_BF16, k_scale=1.0,
+                      v_scale=1.0, workspace=None, stream=None):
+    """pd_decode with sequence b's q heads at q_rows[b, :Hq * D] and its output
+    heads written to out_rows[b, :Hq * D] (both bf16 [B, row] tensors)."""
     B, stride = _strided_q(q_rows, num_q_heads, head_dim)
-    if out.shape != (B, num_q_heads, head_dim):
-        raise ValueError("out must be [num_seqs, num_q_heads, head_dim]")
+    Bo, ostride = _strided_rows(out_rows, num_q_heads, head_dim, "out_rows")
+    if Bo != B:
+        raise ValueError("q_rows and out_rows have different numbers of sequences")
     mbs = block_tables.shape[1]
     code = _dtype_code(kv_dtype)
     S = num_splits
@@ -413,23 +420,25 @@ def pd_decode_strided(q_rows, k_cache, v_cache, block_tables, seq_lens, out, *, 
         _dev(q_rows, "q_rows", torch.bfloat16, dev), stride,
         _dev(k_cache, "k_cache", None, dev), _dev(v_cache, "v_cache", None, dev),
         _dev(block_tables, "block_tables", torch.int32, dev),
-        _dev(seq_lens, "seq_lens", torch.int32, dev), _dev(out, "out", torch.bfloat16, dev), B,
+        _dev(seq_lens, "seq_lens", torch.int32, dev),
+        _dev(out_rows, "out_rows", torch.bfloat16, dev), ostride, B,
         num_q_heads, num_kv_heads, head_dim, block_size, mbs, num_blocks, float(scale), S,
         sliding_window, code, float(k_scale), float(v_scale),
         _dev(workspace, "workspace", None, dev), workspace.numel() * workspace.element_size(),
         _stream(stream))
     _check("pd_decode_strided", rc)
-    return out
+    return out_rows
 
 
-def pd_decode_balanced_strided(q_rows, k_cache, v_cache, block_tables, plan_dev, plan, out, *,
-                               num_q_heads, head_dim, num_kv_heads, block_size, num_blocks,
-                               scale, sliding_window=0, kv_dtype=PD_KV_BF16, k_scale=1.0,
-                               v_scale=1.0, workspace=None, stream=None):
-    """pd_decode_balanced with sequence b's q heads at q_rows[b, :num_q_heads * head_dim]."""
+def pd_decode_balanced_strided(q_rows, k_cache, v_cache, block_tables, plan_dev, plan,
+                               out_rows, *, num_q_heads, head_dim, num_kv_heads, block_size,
+                               num_blocks, scale, sliding_window=0, kv_dtype=PD_KV_BF16,
+                               k_scale=1.0, v_scale=1.0, workspace=None, stream=None):
+    """pd_decode_balanced with strided q rows and output rows (as pd_decode_strided)."""
     B, stride = _strided_q(q_rows, num_q_heads, head_dim)
-    if out.shape != (B, num_q_heads, head_dim):
-        raise ValueError("out must be [num_seqs, num_q_heads, head_dim]")
+    Bo, ostride = _strided_rows(out_rows, num_q_heads, head_dim, "out_rows")
+    if Bo != B:
+        raise ValueError("q_rows and out_rows have different numbers of sequences")
     dev = q_rows.device
     if workspace is None:
         workspace = torch.empty(max(plan.workspace_bytes, 16), dtype=torch.uint8, device=dev)
@@ -438,10 +447,11 @@ def pd_decode_balanced_strided(q_rows, k_cache, v_cache, block_tables, plan_dev,
         _dev(k_cache, "k_cache", None, dev), _dev(v_cache, "v_cache", None, dev),
         _dev(block_tables, "block_tables", torch.int32, dev),
         _dev(plan_dev, "plan", torch.int32, dev), plan_dev.numel() * 4,
-        _dev(out, "out", torch.bfloat16, dev), B, num_q_heads, num_kv_heads, head_dim,
+        _dev(out_rows, "out_rows", torch.bfloat16, dev), ostride, B, num_q_heads, num_kv_heads,
+        head_dim,
         block_size, block_tables.shape[1], num_blocks, float(scale), sliding_window,
         _dtype_code(kv_dtype), float(k_scale), float(v_scale), plan.num_ctas, plan.num_pieces,
         _dev(workspace, "workspace", None, dev), workspace.numel() * workspace.element_size(),
         _stream(stream))
     _check("pd_decode_balanced_strided", rc)
-    return out
+    return out_rows

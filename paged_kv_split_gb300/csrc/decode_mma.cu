@@ -40,6 +40,8 @@
 #include <mutex>
 #include <type_traits>
 
+#include "mma_common.cuh"
+#include "mma_tile.cuh"
 #include "pd_common.cuh"
 
 // Cfg<> defines every layout constant for every form; NVFP4 ignores some.
@@ -48,207 +50,7 @@
 namespace pd {
 namespace {
 
-// Shared-memory budget of the stage ring per CTA (bytes; at least 2 stages):
-// 64 KB lets three CTAs share an SM for head_dim <= 128; the head_dim-split
-// kernels (256 / 512) do better with 96 KB and two CTAs.
-#ifndef PD_MMA_RING_BYTES_SMALL_D
-#define PD_MMA_RING_BYTES_SMALL_D (64 * 1024)
-#endif
-#ifndef PD_MMA_RING_BYTES_LARGE_D
-#define PD_MMA_RING_BYTES_LARGE_D (96 * 1024)
-#endif
-
-constexpr int kConsumerWarps = 4;
-constexpr int kMmaThreads = (kConsumerWarps + 1) * 32;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-
-// ---------------------------------------------------------------------------
-// PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile(
-      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
-          bar),
-      "r"(bytes)
-      : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-// Wait for the phase with the given parity to complete; false after ~2 s.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) return false;
-  }
-  return true;
-}
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            int z, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void consumers_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-template <bool F16>
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  if constexpr (F16) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
-        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  } else {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
-}
-__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
-  uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-// Two E4M3 codes (low byte = first element) -> f16x2 (low half = first). Exact.
-__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two_bytes) {
-  uint32_t r;
-  const uint16_t v = static_cast<uint16_t>(two_bytes);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
-  return r;
-}
-// Four bytes, each two E2M1 codes (low nibble = first element) -> four f16x2.
-__device__ __forceinline__ void e2m1x8_f16x2(uint32_t w, uint32_t (&o)[4]) {
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
-      : "r"(w));
-}
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t x, uint32_t y) {
-  __half2 hx, hy;
-  memcpy(&hx, &x, 4);
-  memcpy(&hy, &y, 4);
-  const __half2 hr = __hmul2(hx, hy);
-  uint32_t r;
-  memcpy(&r, &hr, 4);
-  return r;
-}
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  uint32_t r;
-  memcpy(&r, &h, 4);
-  return r;
-}
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  uint32_t r;
-  memcpy(&r, &h, 4);
-  return r;
-}
-__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
-}
-// Load n bytes (4, 8 or 16) from shared memory into words w[0..n/4).
-template <int N>
-__device__ __forceinline__ void lds_words(uint32_t addr, uint32_t* w) {
-  if constexpr (N == 16) {
-    const uint4 v = lds128(addr);
-    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-  } else if constexpr (N == 8) {
-    const uint2 v = lds64(addr);
-    w[0] = v.x; w[1] = v.y;
-  } else {
-    w[0] = lds32(addr);
-  }
-}
-// 128-byte swizzle of a byte offset inside a 1024-byte aligned region (the
-// pattern TMA writes with CU_TENSOR_MAP_SWIZZLE_128B).
-__device__ __forceinline__ uint32_t swz128(uint32_t off) { return off ^ ((off >> 3) & 0x70u); }
-template <bool ON>
-__device__ __forceinline__ uint32_t swz(uint32_t off) {
-  if constexpr (ON) return swz128(off);
-  return off;
-}
-// 2^e as a float, e clamped to normal exponents.
-__device__ __forceinline__ float exp2i(int e) {
-  e = e < -120 ? -120 : (e > 120 ? 120 : e);
-  return __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
-}
-// floor(log2 |m|) for m > 0 normal; 0 otherwise
-__device__ __forceinline__ int ilog2f(float m) {
-  return m > 0.0f ? static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 127 : 0;
-}
+using namespace ::pd::mma;
 
 // ---------------------------------------------------------------------------
 template <int FMT, int D, int NT, int BS>
@@ -350,7 +152,7 @@ __global__ void __launch_bounds__(kMmaThreads)
   const int P = num_key_pages(L, a.sliding_window, bs);
   if (s * a.chunk >= P) {  // no key of this sequence falls in this split
     if (a.direct && P == 0 && s == 0) {  // an empty sequence: zero output rows
-      uint16_t* o = a.out + (static_cast<int64_t>(b) * a.num_q_heads + g * G) * D;
+      uint16_t* o = a.out + static_cast<int64_t>(b) * a.out_stride + g * G * D;
       for (int e = tid; e < G * D; e += blockDim.x) o[e] = 0;
     }
     return;
@@ -468,81 +270,14 @@ __global__ void __launch_bounds__(kMmaThreads)
   // =========================== consumer warps ==============================
   const int d0 = C::kDSplit == 4 ? warp * C::kDS : 0;  // this warp's head_dim slice
 
-  // ---- q fragments (B operand of S^T = K Q^T), kept in registers ----
-  // BF16: natural order, k index = d. f16 forms: thread column c owns the
-  // slice's d in [c*DS/4, (c+1)*DS/4); k-step ks uses d = c*DS/4 + 4ks + {0..3}.
-  uint32_t qf[C::kKSteps][NT][2];
-  float qmul[NT][2];  // score multiplier (log2 units) of the two head columns of this thread
-  {
-    const uint16_t* qb = a.q + static_cast<int64_t>(b) * a.q_stride + g * G * D;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int n = nt * 8 + r;  // q head row of the B fragment
-      if constexpr (!F16) {
-        qmul[nt][0] = qmul[nt][1] = a.scale_log2;
-#pragma unroll
-        for (int ks = 0; ks < C::kKSteps; ++ks) {
-          uint32_t w0 = 0, w1 = 0;
-          if (n < G) {
-            const uint16_t* p = qb + n * D + d0 + ks * 16 + 2 * c;
-            w0 = *reinterpret_cast<const uint32_t*>(p);
-            w1 = *reinterpret_cast<const uint32_t*>(p + 8);
-          }
-          qf[ks][nt][0] = w0;
-          qf[ks][nt][1] = w1;
-        }
-      } else {
-        // this thread's q values (4 consecutive d per k-step), loaded up front
-        uint2 raw[C::kKSteps];
-#pragma unroll
-        for (int ks = 0; ks < C::kKSteps; ++ks)
-          raw[ks] = (n < G) ? *reinterpret_cast<const uint2*>(qb + n * D + d0 + c * (C::kDS / 4) +
-                                                               4 * ks)
-                            : make_uint2(0u, 0u);
-        // power-of-two scale putting max |q| of head n in [2^14, 2^15)
-        float m = 0.0f;
-#pragma unroll
-        for (int ks = 0; ks < C::kKSteps; ++ks)
-          m = fmaxf(fmaxf(m, fmaxf(fabsf(bf16_lo(raw[ks].x)), fabsf(bf16_hi(raw[ks].x)))),
-                    fmaxf(fabsf(bf16_lo(raw[ks].y)), fabsf(bf16_hi(raw[ks].y))));
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-        if constexpr (C::kDSplit == 4) {  // the other warps hold the rest of head_dim
-          if (c == 0) qmax_s[(nt * 4 + warp) * 8 + r] = m;
-          consumers_sync();
-          m = fmaxf(fmaxf(qmax_s[(nt * 4 + 0) * 8 + r], qmax_s[(nt * 4 + 1) * 8 + r]),
-                    fmaxf(qmax_s[(nt * 4 + 2) * 8 + r], qmax_s[(nt * 4 + 3) * 8 + r]));
-        }
-        const float qdown = exp2i(14 - ilog2f(m));
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const float mj = __shfl_sync(0xFFFFFFFFu, m, (2 * c + j) * 4);
-          qmul[nt][j] = a.scale_log2 * (FMT == PD_KV_FP8_E4M3 ? a.k_scale : 1.0f) *
-                        exp2i(ilog2f(mj) - 14);
-        }
-#pragma unroll
-        for (int ks = 0; ks < C::kKSteps; ++ks) {
-          qf[ks][nt][0] = pack_f16x2(bf16_lo(raw[ks].x) * qdown, bf16_hi(raw[ks].x) * qdown);
-          qf[ks][nt][1] = pack_f16x2(bf16_lo(raw[ks].y) * qdown, bf16_hi(raw[ks].y) * qdown);
-        }
-      }
-    }
-  }
-
-  // ---- running state ----
-  float acc[C::kKSteps][NT][4];  // O^T: [head_dim m-tile][n-tile][fragment]
-#pragma unroll
-  for (int i = 0; i < C::kKSteps; ++i)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[i][nt][k] = 0.0f;
-  float m_run[NT][2], l_run[NT][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    m_run[nt][0] = m_run[nt][1] = -INFINITY;
-    l_run[nt][0] = l_run[nt][1] = 0.0f;
-  }
+  const ThreadPlace tp{warp, lane, r, c, d0};
+  TileState<C, NT> ts;
+  load_q_fragments<FMT, D, NT>(ts, a.q + static_cast<int64_t>(b) * a.q_stride + g * G * D, G,
+                               a.scale_log2, a.k_scale, tp, qmax_s);
+  reset_state(ts);
+  auto& acc = ts.acc;
+  auto& m_run = ts.m_run;
+  auto& l_run = ts.l_run;
 
   bool failed = false;
   int red_buf = 0;
@@ -559,335 +294,7 @@ __global__ void __launch_bounds__(kMmaThreads)
     const uint32_t bad = bad_copies[st];
     const int t0 = t_base + i * C::kKT;
 
-      // ---- scores of one 16-key m-tile over this warp's head_dim slice ----
-      auto qk = [&](const int key0, float (&sc)[NT][4]) {
-        if constexpr (FMT == PD_KV_BF16) {
-          const int mi = lane >> 3, ri = lane & 7;
-          const int key = key0 + ri + 8 * (mi & 1);
-  #pragma unroll
-          for (int ks = 0; ks < C::kKSteps; ++ks) {
-            const int d = d0 + ks * 16 + 8 * (mi >> 1);
-            const uint32_t off = (d / 64) * (C::kKT * 128) + key * 128 + (d % 64) * 2;
-            uint32_t af[4];
-            ldsm_x4(kst + swz128(off), af);
-  #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma16816<false>(sc[nt], af, qf[ks][nt][0], qf[ks][nt][1]);
-          }
-        } else if constexpr (FMT == PD_KV_FP8_E4M3) {
-          // keys key0+r, key0+r+8: bytes d in [c*DS/4, +DS/4) = kKSteps words
-          uint32_t wa[C::kKSteps], wb[C::kKSteps];
-          const int dbyte = d0 + c * (C::kDS / 4);
-          const uint32_t base = (dbyte / C::kCRB) * (C::kKT * C::kCRB) + (dbyte % C::kCRB);
-  #pragma unroll
-          for (int q4 = 0; q4 < C::kKSteps / 4; ++q4) {
-            const uint32_t offa = base + (key0 + r) * C::kCRB + 16 * q4;
-            lds_words<16>(kst + swz<C::kSwizzle>(offa), wa + 4 * q4);
-            lds_words<16>(kst + swz<C::kSwizzle>(offa + 8 * C::kCRB), wb + 4 * q4);
-          }
-  #pragma unroll
-          for (int ks = 0; ks < C::kKSteps; ++ks) {
-            uint32_t af[4];
-            af[0] = e4m3x2_f16x2(wa[ks] & 0xFFFFu);
-            af[1] = e4m3x2_f16x2(wb[ks] & 0xFFFFu);
-            af[2] = e4m3x2_f16x2(wa[ks] >> 16);
-            af[3] = e4m3x2_f16x2(wb[ks] >> 16);
-  #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma16816<true>(sc[nt], af, qf[ks][nt][0], qf[ks][nt][1]);
-          }
-        } else {  // NVFP4
-          constexpr int kB = C::kDS / 8;  // data bytes of this thread's slice per key (8|16)
-          const int dn = d0 + c * (C::kDS / 4);
-          const uint32_t offa = (key0 + r) * (D / 2) + dn / 2;
-          uint32_t wa[kB / 4], wb[kB / 4];
-          lds_words<kB>(kst + offa, wa);
-          lds_words<kB>(kst + offa + 8 * (D / 2), wb);
-          // one E4M3 scale per 16 elements: k-steps 4j..4j+3 use this slice's group j
-          uint32_t sa[C::kKSteps / 4], sbv[C::kKSteps / 4];
-          const uint32_t soa = C::kDataBytes + (key0 + r) * (D / 16) + dn / 16;
-  #pragma unroll
-          for (int j = 0; j < C::kKSteps / 4; ++j) {
-            const uint32_t xa = lds_u8(kst + soa + j);
-            const uint32_t xb = lds_u8(kst + soa + 8 * (D / 16) + j);
-            sa[j] = e4m3x2_f16x2(xa | (xa << 8));
-            sbv[j] = e4m3x2_f16x2(xb | (xb << 8));
-          }
-  #pragma unroll
-          for (int w = 0; w < kB / 4; ++w) {
-            uint32_t xa[4], xb[4];
-            e2m1x8_f16x2(wa[w], xa);
-            e2m1x8_f16x2(wb[w], xb);
-            // byte 2h of word w -> k-step 2w+h, d +{0,1}; byte 2h+1 -> d +{2,3}
-  #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int ks = 2 * w + h;
-              const int grp = ks / 4;
-              uint32_t af[4];
-              af[0] = hmul2_u32(xa[2 * h], sa[grp]);
-              af[1] = hmul2_u32(xb[2 * h], sbv[grp]);
-              af[2] = hmul2_u32(xa[2 * h + 1], sa[grp]);
-              af[3] = hmul2_u32(xb[2 * h + 1], sbv[grp]);
-  #pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-                mma16816<true>(sc[nt], af, qf[ks][nt][0], qf[ks][nt][1]);
-            }
-          }
-        }
-
-      };
-      // ---- O^T += V^T P^T for one m-tile (masked keys' V halves zeroed) ----
-      // MASKED: the m-tile is ragged, keep_lo / keep_hi zero the V halves of masked keys
-      auto pv = [&](auto masked, const int key0, const uint32_t (&pbf)[NT][2],
-                    const uint32_t keep_lo, const uint32_t keep_hi) {
-        constexpr bool kMasked = decltype(masked)::value;
-        if constexpr (FMT == PD_KV_BF16) {
-          const int mi = lane >> 3, ri = lane & 7;
-          const int key = key0 + ri + 8 * (mi >> 1);
-  #pragma unroll
-          for (int md = 0; md < C::kKSteps; ++md) {
-            const int d = d0 + md * 16 + 8 * (mi & 1);
-            const uint32_t off = (d / 64) * (C::kKT * 128) + key * 128 + (d % 64) * 2;
-            uint32_t af[4];
-            ldsm_x4_trans(vst + swz128(off), af);
-            if constexpr (kMasked) {
-              af[0] &= keep_lo;
-              af[1] &= keep_lo;
-              af[2] &= keep_hi;
-              af[3] &= keep_hi;
-            }
-  #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma16816<false>(acc[md][nt], af, pbf[nt][0], pbf[nt][1]);
-          }
-        } else if constexpr (FMT == PD_KV_FP8_E4M3) {
-          // V bytes d in [r*DS/8, (r+1)*DS/8) of keys 2c, 2c+1, 2c+8, 2c+9; byte j is
-          // head_dim row (m-tile j, row r) for j < DS/16 and (j - DS/16, row r+8) above
-          constexpr int kVB = C::kDS / 8;  // 16 or 8
-          const int dbyte = d0 + r * kVB;
-          const uint32_t base = (dbyte / C::kCRB) * (C::kKT * C::kCRB) + (dbyte % C::kCRB);
-          uint32_t v[4][kVB / 4];
-  #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const int key = key0 + 2 * c + (k4 & 1) + 8 * (k4 >> 1);
-            lds_words<kVB>(vst + swz<C::kSwizzle>(base + key * C::kCRB), v[k4]);
-          }
-          // interleave the bytes of the key pairs: PRMT gives {a_j, b_j, a_j+1, b_j+1}
-          uint32_t pr01[kVB / 2], pr23[kVB / 2];
-  #pragma unroll
-          for (int w = 0; w < kVB / 4; ++w) {
-            pr01[2 * w] = __byte_perm(v[0][w], v[1][w], 0x5140);
-            pr01[2 * w + 1] = __byte_perm(v[0][w], v[1][w], 0x7362);
-            pr23[2 * w] = __byte_perm(v[2][w], v[3][w], 0x5140);
-            pr23[2 * w + 1] = __byte_perm(v[2][w], v[3][w], 0x7362);
-          }
-          // byte pair j sits in pr[j / 2], half j % 2
-  #pragma unroll
-          for (int md = 0; md < C::kKSteps; ++md) {
-            const int jl = md, jh = md + C::kKSteps;
-            uint32_t af[4];
-            af[0] = e4m3x2_f16x2(pr01[jl >> 1] >> (16 * (jl & 1)));
-            af[1] = e4m3x2_f16x2(pr01[jh >> 1] >> (16 * (jh & 1)));
-            af[2] = e4m3x2_f16x2(pr23[jl >> 1] >> (16 * (jl & 1)));
-            af[3] = e4m3x2_f16x2(pr23[jh >> 1] >> (16 * (jh & 1)));
-            if constexpr (kMasked) {
-              af[0] &= keep_lo;
-              af[1] &= keep_lo;
-              af[2] &= keep_hi;
-              af[3] &= keep_hi;
-            }
-  #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma16816<true>(acc[md][nt], af, pbf[nt][0], pbf[nt][1]);
-          }
-        } else {  // NVFP4
-          // V nibbles d in [r*DS/8, (r+1)*DS/8) of keys 2c, 2c+1, 2c+8, 2c+9 (one scale
-          // group per key); nibble j is head_dim row (j, r) below DS/16, else (j - DS/16, r+8)
-          constexpr int kVB = C::kDS / 16;  // data bytes per key (8 or 4)
-          const int dn = d0 + r * (C::kDS / 8);
-          uint32_t v[4][2];
-          uint32_t sv[4];
-  #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const int key = key0 + 2 * c + (k4 & 1) + 8 * (k4 >> 1);
-            v[k4][1] = 0u;
-            lds_words<kVB>(vst + key * (D / 2) + dn / 2, v[k4]);
-            sv[k4] = lds_u8(vst + C::kDataBytes + key * (D / 16) + dn / 16);
-          }
-          const uint32_t s01 = e4m3x2_f16x2(sv[0] | (sv[1] << 8));
-          const uint32_t s23 = e4m3x2_f16x2(sv[2] | (sv[3] << 8));
-          // pair bytes (a_j | b_j << 4): even j from the low nibbles, odd j from the high
-          uint32_t f01[2 * kVB], f23[2 * kVB];  // f16x2 per nibble index j
-  #pragma unroll
-          for (int w = 0; w < kVB / 4; ++w) {
-            const uint32_t e01 = (v[0][w] & 0x0F0F0F0Fu) | ((v[1][w] & 0x0F0F0F0Fu) << 4);
-            const uint32_t o01 = ((v[0][w] >> 4) & 0x0F0F0F0Fu) | (v[1][w] & 0xF0F0F0F0u);
-            const uint32_t e23 = (v[2][w] & 0x0F0F0F0Fu) | ((v[3][w] & 0x0F0F0F0Fu) << 4);
-            const uint32_t o23 = ((v[2][w] >> 4) & 0x0F0F0F0Fu) | (v[3][w] & 0xF0F0F0F0u);
-            uint32_t t[4];
-            e2m1x8_f16x2(e01, t);
-  #pragma unroll
-            for (int k = 0; k < 4; ++k) f01[8 * w + 2 * k] = hmul2_u32(t[k], s01);
-            e2m1x8_f16x2(o01, t);
-  #pragma unroll
-            for (int k = 0; k < 4; ++k) f01[8 * w + 2 * k + 1] = hmul2_u32(t[k], s01);
-            e2m1x8_f16x2(e23, t);
-  #pragma unroll
-            for (int k = 0; k < 4; ++k) f23[8 * w + 2 * k] = hmul2_u32(t[k], s23);
-            e2m1x8_f16x2(o23, t);
-  #pragma unroll
-            for (int k = 0; k < 4; ++k) f23[8 * w + 2 * k + 1] = hmul2_u32(t[k], s23);
-          }
-  #pragma unroll
-          for (int md = 0; md < C::kKSteps; ++md) {
-            uint32_t af[4];
-            af[0] = f01[md];
-            af[1] = f01[md + C::kKSteps];
-            af[2] = f23[md];
-            af[3] = f23[md + C::kKSteps];
-            if constexpr (kMasked) {
-              af[0] &= keep_lo;
-              af[1] &= keep_lo;
-              af[2] &= keep_hi;
-              af[3] &= keep_hi;
-            }
-  #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma16816<true>(acc[md][nt], af, pbf[nt][0], pbf[nt][1]);
-          }
-        }
-      };
-      auto key_ok = [&](int kk) {  // kk: key index within the stage
-        const int kabs = t0 + kk;
-        return kabs >= t_begin && kabs < t_end && !((bad >> (kk / C::kBR)) & 1u);
-      };
-      // m-tiles this warp handles in this stage: its own kWM (keys split across
-      // warps) or all of them (head_dim split across warps)
-      constexpr int kU = C::kDSplit == 1 ? C::kWM : C::kMT;
-      auto mt_of = [&](int u) { return C::kDSplit == 1 ? warp * C::kWM + u : u; };
-
-      float sc[kU][NT][4];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) sc[u][nt][0] = sc[u][nt][1] = sc[u][nt][2] = sc[u][nt][3] = 0.0f;
-        qk(mt_of(u) * 16, sc[u]);
-      }
-
-      // ---------------- sum the head_dim slices (head_dim 256/512) ----------
-      if constexpr (C::kDSplit == 4) {
-        float* mine = red + (red_buf * 4 + warp) * (kU * NT * 32 * 4);
-#pragma unroll
-        for (int u = 0; u < kU; ++u)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            *reinterpret_cast<float4*>(mine + ((u * NT + nt) * 32 + lane) * 4) =
-                make_float4(sc[u][nt][0], sc[u][nt][1], sc[u][nt][2], sc[u][nt][3]);
-        consumers_sync();
-#pragma unroll
-        for (int u = 0; u < kU; ++u)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const float4 v = *reinterpret_cast<const float4*>(
-                  red + (red_buf * 4 + w) * (kU * NT * 32 * 4) + ((u * NT + nt) * 32 + lane) * 4);
-              t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
-            }
-            sc[u][nt][0] = t.x; sc[u][nt][1] = t.y; sc[u][nt][2] = t.z; sc[u][nt][3] = t.w;
-          }
-      }
-
-      // ---------------- mask, scale, one online-softmax update ----------------
-      // fragment rows r (c0,c1) and r+8 (c2,c3) of m-tile u are keys 16*mt + r, +8
-      // an m-tile is ragged if any of its 16 keys is masked (warp-uniform)
-      bool ragged[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int key0 = mt_of(u) * 16;
-        ragged[u] = (t0 + key0 < t_begin) || (t0 + key0 + 16 > t_end) ||
-                    ((bad >> (key0 / C::kBR)) & 1u);
-      }
-      float p[kU][NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const int key0 = mt_of(u) * 16;
-          const bool va = !ragged[u] || key_ok(key0 + r);
-          const bool vb = !ragged[u] || key_ok(key0 + r + 8);
-          p[u][nt][0] = va ? sc[u][nt][0] * qmul[nt][0] : -INFINITY;
-          p[u][nt][1] = va ? sc[u][nt][1] * qmul[nt][1] : -INFINITY;
-          p[u][nt][2] = vb ? sc[u][nt][2] * qmul[nt][0] : -INFINITY;
-          p[u][nt][3] = vb ? sc[u][nt][3] * qmul[nt][1] : -INFINITY;
-          mx0 = fmaxf(mx0, fmaxf(p[u][nt][0], p[u][nt][2]));
-          mx1 = fmaxf(mx1, fmaxf(p[u][nt][1], p[u][nt][3]));
-        }
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, o));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, o));
-        }
-        const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
-        // the running max of no column moved: every factor is exactly 1, skip the rescale
-        const bool grew = __any_sync(0xFFFFFFFFu, mn0 > m_run[nt][0] || mn1 > m_run[nt][1]);
-        const float al0 = (mn0 == -INFINITY) ? 1.0f : ex2(m_run[nt][0] - mn0);
-        const float al1 = (mn1 == -INFINITY) ? 1.0f : ex2(m_run[nt][1] - mn1);
-        m_run[nt][0] = mn0;
-        m_run[nt][1] = mn1;
-        float ls0 = 0.0f, ls1 = 0.0f;
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          p[u][nt][0] = (mn0 == -INFINITY) ? 0.0f : ex2(p[u][nt][0] - mn0);
-          p[u][nt][1] = (mn1 == -INFINITY) ? 0.0f : ex2(p[u][nt][1] - mn1);
-          p[u][nt][2] = (mn0 == -INFINITY) ? 0.0f : ex2(p[u][nt][2] - mn0);
-          p[u][nt][3] = (mn1 == -INFINITY) ? 0.0f : ex2(p[u][nt][3] - mn1);
-          ls0 += p[u][nt][0] + p[u][nt][2];
-          ls1 += p[u][nt][1] + p[u][nt][3];
-        }
-        if (grew) {
-          l_run[nt][0] *= al0;
-          l_run[nt][1] *= al1;
-#pragma unroll
-          for (int md = 0; md < C::kKSteps; ++md) {
-            acc[md][nt][0] *= al0;
-            acc[md][nt][1] *= al1;
-            acc[md][nt][2] *= al0;
-            acc[md][nt][3] *= al1;
-          }
-        }
-        l_run[nt][0] += ls0;
-        l_run[nt][1] += ls1;
-      }
-
-      // ---------------- O^T += V^T P^T, m-tile by m-tile ----------------
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int key0 = mt_of(u) * 16;
-        // P^T as B fragments: the 8x8 blocks have keys as rows, q heads as columns
-        uint32_t pbf[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const uint32_t top = F16 ? pack_f16x2(p[u][nt][0], p[u][nt][1])
-                                   : pack_bf16x2(p[u][nt][0], p[u][nt][1]);
-          const uint32_t bot = F16 ? pack_f16x2(p[u][nt][2], p[u][nt][3])
-                                   : pack_bf16x2(p[u][nt][2], p[u][nt][3]);
-          pbf[nt][0] = movmatrix_trans(top);
-          pbf[nt][1] = movmatrix_trans(bot);
-        }
-        if (ragged[u]) {
-          const uint32_t keep_lo = (key_ok(key0 + 2 * c) ? 0x0000FFFFu : 0u) |
-                                   (key_ok(key0 + 2 * c + 1) ? 0xFFFF0000u : 0u);
-          const uint32_t keep_hi = (key_ok(key0 + 2 * c + 8) ? 0x0000FFFFu : 0u) |
-                                   (key_ok(key0 + 2 * c + 9) ? 0xFFFF0000u : 0u);
-          pv(std::true_type{}, key0, pbf, keep_lo, keep_hi);
-        } else {
-          pv(std::false_type{}, key0, pbf, 0u, 0u);
-        }
-      }
-
+    consume_tile<FMT, D, NT>(ts, StageView{kst, vst, t0, t_begin, t_end, bad}, tp, red, red_buf);
     if constexpr (C::kDSplit == 4) red_buf ^= 1;
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
@@ -910,7 +317,7 @@ __global__ void __launch_bounds__(kMmaThreads)
   };
   const int64_t row0 = (static_cast<int64_t>(b) * a.num_q_heads + g * G) * a.num_splits + s;
 
-  const int64_t orow0 = (static_cast<int64_t>(b) * a.num_q_heads + g * G) * D;  // out row of head 0
+  const int64_t orow0 = static_cast<int64_t>(b) * a.out_stride + g * G * D;  // out row of head 0
   if constexpr (C::kDSplit == 4) {
     // every warp holds the same (m, l) and its own head_dim slice of O
     if (!failed) {
@@ -988,49 +395,6 @@ __global__ void __launch_bounds__(kMmaThreads)
       }
     }
   }
-}
-
-// ---------------------------------------------------------------------------
-// Host side: tensor maps and launch.
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static std::once_flag once;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  std::call_once(once, []() {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// 3-D map over a BF16 / FP8 cache: dims (d, kv head, pool row), box
-// (copy_elems, 1, rows), 128-byte swizzle for 128-byte rows.
-bool encode_cache_map(CUtensorMap* m, const void* base, int kv_dtype, int D, int hkv,
-                      int64_t pool_rows, int copy_elems, int rows, bool swizzle) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const int esz = kv_dtype == PD_KV_BF16 ? 2 : 1;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(hkv),
-                              static_cast<cuuint64_t>(pool_rows)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * esz,
-                                 static_cast<cuuint64_t>(hkv) * D * esz};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(copy_elems), 1u,
-                             static_cast<cuuint32_t>(rows)};
-  const cuuint32_t estr[3] = {1u, 1u, 1u};
-  const CUresult rc = fn(
-      m, esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
-      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-      swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-      // L2 fills no wider than one head's row: a wider fill would pull in the
-      // next head's bytes, which another CTA reads at some other time
-      D * esz >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
-                     : (D * esz >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
-                                       : CU_TENSOR_MAP_L2_PROMOTION_L2_64B),
-      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return rc == CUDA_SUCCESS;
 }
 
 template <int FMT, int D, int NT, int BS>

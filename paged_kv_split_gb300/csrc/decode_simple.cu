@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
                         (static_cast<uint32_t>(f32_to_bf16(acc.y * inv)) << 16);
   const uint32_t lo23 = static_cast<uint32_t>(f32_to_bf16(acc.z * inv)) |
                         (static_cast<uint32_t>(f32_to_bf16(acc.w * inv)) << 16);
-  *reinterpret_cast<uint2*>(a.out + (static_cast<int64_t>(b) * a.num_q_heads + h) * D + d) =
+  *reinterpret_cast<uint2*>(a.out + static_cast<int64_t>(b) * a.out_stride + h * D + d) =
       make_uint2(lo01, lo23);
 }
 

@@ -1,0 +1,274 @@
+// Building blocks shared by the tensor-core partial kernels (decode_mma.cu,
+// decode_balanced.cu): PTX wrappers for mbarriers, TMA and bulk copies,
+// ldmatrix / mma.sync / movmatrix and the E4M3 / E2M1 conversions, the
+// bounded waits, and the host-side tensor-map encoding of a paged cache.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "pd_common.cuh"
+
+namespace pd {
+namespace mma {
+
+// Shared-memory budget of the stage ring per CTA (bytes; at least 2 stages):
+// 64 KB lets three CTAs share an SM for head_dim <= 128; the head_dim-split
+// kernels (256 / 512) do better with 96 KB and two CTAs.
+#ifndef PD_MMA_RING_BYTES_SMALL_D
+#define PD_MMA_RING_BYTES_SMALL_D (64 * 1024)
+#endif
+#ifndef PD_MMA_RING_BYTES_LARGE_D
+#define PD_MMA_RING_BYTES_LARGE_D (96 * 1024)
+#endif
+
+constexpr int kConsumerWarps = 4;
+constexpr int kMmaThreads = (kConsumerWarps + 1) * 32;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+          bar),
+      "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the phase with the given parity to complete; false after ~2 s.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+// The same wait taken by a whole warp with one outcome for all its lanes
+// (false if any lane ran out of time or `abort_flag` is set), so that the
+// warp never splits on a wait that ends near its limit.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
+                                          const volatile int* abort_flag) {
+  (void)abort_flag;
+  return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity));
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  if constexpr (F16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Two E4M3 codes (low byte = first element) -> f16x2 (low half = first). Exact.
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two_bytes) {
+  uint32_t r;
+  const uint16_t v = static_cast<uint16_t>(two_bytes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+// Four bytes, each two E2M1 codes (low nibble = first element) -> four f16x2.
+__device__ __forceinline__ void e2m1x8_f16x2(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+}
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t x, uint32_t y) {
+  __half2 hx, hy;
+  memcpy(&hx, &x, 4);
+  memcpy(&hy, &y, 4);
+  const __half2 hr = __hmul2(hx, hy);
+  uint32_t r;
+  memcpy(&r, &hr, 4);
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  uint32_t r;
+  memcpy(&r, &h, 4);
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  uint32_t r;
+  memcpy(&r, &h, 4);
+  return r;
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+// Load n bytes (4, 8 or 16) from shared memory into words w[0..n/4).
+template <int N>
+__device__ __forceinline__ void lds_words(uint32_t addr, uint32_t* w) {
+  if constexpr (N == 16) {
+    const uint4 v = lds128(addr);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else if constexpr (N == 8) {
+    const uint2 v = lds64(addr);
+    w[0] = v.x; w[1] = v.y;
+  } else {
+    w[0] = lds32(addr);
+  }
+}
+// 128-byte swizzle of a byte offset inside a 1024-byte aligned region (the
+// pattern TMA writes with CU_TENSOR_MAP_SWIZZLE_128B).
+__device__ __forceinline__ uint32_t swz128(uint32_t off) { return off ^ ((off >> 3) & 0x70u); }
+template <bool ON>
+__device__ __forceinline__ uint32_t swz(uint32_t off) {
+  if constexpr (ON) return swz128(off);
+  return off;
+}
+// 2^e as a float, e clamped to normal exponents.
+__device__ __forceinline__ float exp2i(int e) {
+  e = e < -120 ? -120 : (e > 120 ? 120 : e);
+  return __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+}
+// floor(log2 |m|) for m > 0 normal; 0 otherwise
+__device__ __forceinline__ int ilog2f(float m) {
+  return m > 0.0f ? static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 127 : 0;
+}
+
+// ---------------------------------------------------------------------------
+// Host side: tensor maps.
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a BF16 / FP8 cache: dims (d, kv head, pool row), box
+// (copy_elems, 1, rows), 128-byte swizzle for 128-byte rows.
+inline bool encode_cache_map(CUtensorMap* m, const void* base, int kv_dtype, int D, int hkv,
+                      int64_t pool_rows, int copy_elems, int rows, bool swizzle) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int esz = kv_dtype == PD_KV_BF16 ? 2 : 1;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(hkv),
+                              static_cast<cuuint64_t>(pool_rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * esz,
+                                 static_cast<cuuint64_t>(hkv) * D * esz};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(copy_elems), 1u,
+                             static_cast<cuuint32_t>(rows)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult rc = fn(
+      m, esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+      // L2 fills no wider than one head's row: a wider fill would pull in the
+      // next head's bytes, which another CTA reads at some other time
+      D * esz >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                     : (D * esz >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                       : CU_TENSOR_MAP_L2_PROMOTION_L2_64B),
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rc == CUDA_SUCCESS;
+}
+
+}  // namespace mma
+}  // namespace pd

@@ -94,6 +94,7 @@ DecodeArgs make_decode_args(const DecodeShape& s, const void* q, const void* kc,
   a.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + ws_o_bytes(s.B, s.Hq, s.D, s.S));
   a.flags = flags;
   a.out = nullptr;
+  a.out_stride = static_cast<int64_t>(s.Hq) * s.D;
   a.direct = 0;
   a.num_blocks = s.nb;
   a.page_bytes = page_bytes_of(s.kv_dtype, s.bs, s.Hkv, s.D);
@@ -124,6 +125,7 @@ CombineArgs make_combine_args(int B, int Hq, int D, int bs, int mbs, int S, int 
   c.ws_ml = reinterpret_cast<const float2*>(static_cast<const char*>(ws) + ws_o_bytes(B, Hq, D, S));
   c.seq_lens = lens;
   c.out = static_cast<uint16_t*>(out);
+  c.out_stride = static_cast<int64_t>(Hq) * D;
   c.num_seqs = B;
   c.num_q_heads = Hq;
   c.block_size = bs;
@@ -558,8 +560,9 @@ int decode_split(const void* q, const void* k_cache, const void* v_cache,
                  int32_t block_size, int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
                  int32_t num_splits, int32_t sliding_window, int32_t kv_dtype, float k_scale,
                  float v_scale, void* workspace, size_t workspace_bytes, void* stream,
-                 int64_t q_stride) {
+                 int64_t q_stride, int64_t out_stride = 0) {
   if (!q_stride_ok(q_stride, num_q_heads, head_dim)) return PD_ERR_INVALID_ARG;
+  if (!q_stride_ok(out_stride, num_q_heads, head_dim)) return PD_ERR_INVALID_ARG;
   if (num_splits < 0 || num_splits > kMaxSplits) return PD_ERR_INVALID_ARG;
   if (num_seqs > 0 && !dev_ptr_ok(out)) return PD_ERR_INVALID_ARG;
   int S = num_splits;
@@ -578,8 +581,12 @@ int decode_split(const void* q, const void* k_cache, const void* v_cache,
                           scale, S, sliding_window, kv_dtype, k_scale, v_scale, workspace,
                           workspace_bytes, stream, q_stride);
     if (rc != PD_OK || num_seqs == 0) return rc;
-    return pd_decode_combine(workspace, workspace_bytes, seq_lens, out, num_seqs, num_q_heads,
-                             head_dim, block_size, max_blocks_per_seq, S, sliding_window, stream);
+    if (!dev_ptr_ok(out)) return PD_ERR_INVALID_ARG;
+    CombineArgs c = make_combine_args(num_seqs, num_q_heads, head_dim, block_size,
+                                      max_blocks_per_seq, S, sliding_window, workspace, seq_lens,
+                                      out);
+    if (out_stride) c.out_stride = out_stride;
+    return cuda_status(launch_decode_combine(c, head_dim, static_cast<cudaStream_t>(stream)));
   }
   // the partial kernel writes the rows of sequences whose keys fit one split
   // (and zero rows for empty ones); the combine merges the rest
@@ -596,12 +603,14 @@ int decode_split(const void* q, const void* k_cache, const void* v_cache,
   a.out = static_cast<uint16_t*>(out);
   a.direct = 1;
   if (q_stride) a.q_stride = q_stride;
+  if (out_stride) a.out_stride = out_stride;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_decode_partial_mma(a, head_dim, kv_dtype, st) != cudaSuccess) return PD_ERR_CUDA;
   CombineArgs c = make_combine_args(num_seqs, num_q_heads, head_dim, block_size,
                                     max_blocks_per_seq, S, sliding_window, workspace, seq_lens,
                                     out);
   c.skip_direct = 1;
+  if (out_stride) c.out_stride = out_stride;
   return cuda_status(launch_decode_combine(c, head_dim, st));
 }
 }  // namespace
@@ -622,16 +631,17 @@ int pd_decode(const void* q, const void* k_cache, const void* v_cache, const int
 
 int pd_decode_strided(const void* q, int64_t q_stride, const void* k_cache, const void* v_cache,
                       const int32_t* block_tables, const int32_t* seq_lens, void* out,
-                      int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                      int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
-                      int64_t num_blocks, float scale, int32_t num_splits, int32_t sliding_window,
-                      int32_t kv_dtype, float k_scale, float v_scale, void* workspace,
-                      size_t workspace_bytes, void* stream) {
-  if (q_stride <= 0) return PD_ERR_INVALID_ARG;
+                      int64_t out_stride, int32_t num_seqs, int32_t num_q_heads,
+                      int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                      int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
+                      int32_t num_splits, int32_t sliding_window, int32_t kv_dtype,
+                      float k_scale, float v_scale, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  if (q_stride <= 0 || out_stride <= 0) return PD_ERR_INVALID_ARG;
   return decode_split(q, k_cache, v_cache, block_tables, seq_lens, out, num_seqs, num_q_heads,
                       num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
                       num_splits, sliding_window, kv_dtype, k_scale, v_scale, workspace,
-                      workspace_bytes, stream, q_stride);
+                      workspace_bytes, stream, q_stride, out_stride);
 }
 
 int pd_prefer_balanced(const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
@@ -688,8 +698,9 @@ int decode_balanced(const void* q, const void* k_cache, const void* v_cache,
                     int64_t num_blocks, float scale, int32_t sliding_window, int32_t kv_dtype,
                     float k_scale, float v_scale, int32_t num_ctas, int32_t num_pieces,
                     void* workspace, size_t workspace_bytes, void* stream, bool partial,
-                    bool combine, int64_t q_stride = 0) {
+                    bool combine, int64_t q_stride = 0, int64_t out_stride = 0) {
   if (!q_stride_ok(q_stride, num_q_heads, head_dim)) return PD_ERR_INVALID_ARG;
+  if (!q_stride_ok(out_stride, num_q_heads, head_dim)) return PD_ERR_INVALID_ARG;
   // shape checks shared with pd_decode (S = 1 stands for the split count)
   const DecodeShape sh{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                        max_blocks_per_seq, 1, sliding_window, kv_dtype, num_blocks};
@@ -724,6 +735,7 @@ int decode_balanced(const void* q, const void* k_cache, const void* v_cache,
   a.plan_num_ctas = num_ctas;
   a.plan_num_pieces = num_pieces;
   if (q_stride) a.q_stride = q_stride;
+  if (out_stride) a.out_stride = out_stride;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (partial && launch_decode_partial_balanced(a, head_dim, kv_dtype, st) != cudaSuccess)
     return PD_ERR_CUDA;
@@ -735,6 +747,7 @@ int decode_balanced(const void* q, const void* k_cache, const void* v_cache,
   c.ws_ml = a.ws_ml;
   c.plan_seg = pl + lay.seg_off;
   c.num_kv_heads = num_kv_heads;
+  if (out_stride) c.out_stride = out_stride;
   return cuda_status(launch_decode_combine(c, head_dim, st));
 }
 }  // namespace
@@ -757,18 +770,20 @@ int pd_decode_balanced(const void* q, const void* k_cache, const void* v_cache,
 
 int pd_decode_balanced_strided(const void* q, int64_t q_stride, const void* k_cache,
                                const void* v_cache, const int32_t* block_tables,
-                               const void* plan, size_t plan_bytes, void* out, int32_t num_seqs,
+                               const void* plan, size_t plan_bytes, void* out,
+                               int64_t out_stride, int32_t num_seqs,
                                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                int32_t block_size, int32_t max_blocks_per_seq,
                                int64_t num_blocks, float scale, int32_t sliding_window,
                                int32_t kv_dtype, float k_scale, float v_scale, int32_t num_ctas,
                                int32_t num_pieces, void* workspace, size_t workspace_bytes,
                                void* stream) {
-  if (q_stride <= 0) return PD_ERR_INVALID_ARG;
+  if (q_stride <= 0 || out_stride <= 0) return PD_ERR_INVALID_ARG;
   return decode_balanced(q, k_cache, v_cache, block_tables, plan, plan_bytes, out, num_seqs,
                          num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                          num_blocks, scale, sliding_window, kv_dtype, k_scale, v_scale, num_ctas,
-                         num_pieces, workspace, workspace_bytes, stream, true, true, q_stride);
+                         num_pieces, workspace, workspace_bytes, stream, true, true, q_stride,
+                         out_stride);
 }
 
 int pd_decode_balanced_partial(const void* q, const void* k_cache, const void* v_cache,

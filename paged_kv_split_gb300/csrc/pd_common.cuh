@@ -144,7 +144,9 @@ struct DecodeArgs {
   float* ws_o;                   // [B][Hq][S][D]
   float2* ws_ml;                 // [B][Hq][S]
   int* flags;                    // device status word
-  uint16_t* out;                 // [B][Hq][D] bf16 output (used when direct != 0)
+  uint16_t* out;                 // [B][Hq][D] bf16 output (used when direct != 0),
+                                 // sequence b's rows at b * out_stride
+  int64_t out_stride;            // elements between consecutive sequences' output rows
   int direct;                    // 1: a sequence whose keys fit one split writes out
                                  // itself (and an empty one zero rows); the combine
                                  // then skips those sequences
@@ -166,7 +168,8 @@ struct CombineArgs {
   const float* ws_o;
   const float2* ws_ml;
   const int32_t* seq_lens;
-  uint16_t* out;
+  uint16_t* out;                 // sequence b's rows at b * out_stride
+  int64_t out_stride;
   int num_seqs, num_q_heads, block_size, max_blocks_per_seq, num_splits, chunk, sliding_window;
   int skip_direct;               // 1: sequences with one key-holding split are already written
   // balanced plan: per (sequence, kv head) its first piece and piece count;
