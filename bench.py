@@ -40,6 +40,8 @@ ELEM_BYTES = {0: 2.0, 1: 1.0, 2: 0.5625}
 DTYPE_NAME = {0: "bf16", 1: "fp8_e4m3", 2: "nvfp4"}
 PARTIAL_KERNEL_SRC = ["paged_kv_split_gb300/csrc/decode_mma.cu",
                       "paged_kv_split_gb300/csrc/decode_balanced.cu",
+                      "paged_kv_split_gb300/csrc/mma_tile.cuh",
+                      "paged_kv_split_gb300/csrc/mma_common.cuh",
                       "paged_kv_split_gb300/csrc/pd_common.cuh"]
 
 
