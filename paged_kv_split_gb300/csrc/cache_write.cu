@@ -85,6 +85,10 @@ __global__ void __launch_bounds__(kWriteThreads)
                              const int32_t* __restrict__ slots, int hkv, int d, int bs,
                              int64_t num_blocks, float k_scale, float v_scale, int64_t page_bytes,
                              int64_t data_bytes, int* flags) {
+  // Launched as a programmatic dependent of the previous work on the stream
+  // (the previous step's combine, say): nothing global is touched before that
+  // grid has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x;
   const int64_t slot = slots[t];
   if (slot < 0) return;
@@ -109,6 +113,9 @@ __global__ void __launch_bounds__(kWriteThreads)
     quant_row_nvfp4(ksrc, kpage, hkv, d, bs, row, data_bytes);
     quant_row_nvfp4(vsrc, vpage, hkv, d, bs, row, data_bytes);
   }
+  // the decode that reads these rows may now be placed; it still waits for
+  // this grid's completion (griddepcontrol.wait) before its first read
+  asm volatile("griddepcontrol.launch_dependents;");
 }
 
 // max |x| over bf16 values: grid-stride over 16-byte chunks, warp and block
@@ -152,22 +159,29 @@ cudaError_t launch_reshape_and_cache(const uint16_t* key, const uint16_t* value,
   if (T == 0) return cudaSuccess;
   const int64_t pb = page_bytes_of(kv_dtype, bs, hkv, d);
   const int64_t db = nvfp4_data_bytes(bs, hkv, d);
-  const dim3 grid(T), block(kWriteThreads);
+  // a programmatic dependent of the previous work on the stream, like the
+  // decode kernels
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(T);
+  cfg.blockDim = dim3(kWriteThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   switch (kv_dtype) {
     case PD_KV_BF16:
-      reshape_and_cache_kernel<PD_KV_BF16><<<grid, block, 0, st>>>(
-          key, value, kc, vc, slots, hkv, d, bs, nb, k_scale, v_scale, pb, db, flags);
-      break;
+      return cudaLaunchKernelEx(&cfg, reshape_and_cache_kernel<PD_KV_BF16>, key, value, kc, vc,
+                                slots, hkv, d, bs, nb, k_scale, v_scale, pb, db, flags);
     case PD_KV_FP8_E4M3:
-      reshape_and_cache_kernel<PD_KV_FP8_E4M3><<<grid, block, 0, st>>>(
-          key, value, kc, vc, slots, hkv, d, bs, nb, k_scale, v_scale, pb, db, flags);
-      break;
+      return cudaLaunchKernelEx(&cfg, reshape_and_cache_kernel<PD_KV_FP8_E4M3>, key, value, kc,
+                                vc, slots, hkv, d, bs, nb, k_scale, v_scale, pb, db, flags);
     default:
-      reshape_and_cache_kernel<PD_KV_NVFP4><<<grid, block, 0, st>>>(
-          key, value, kc, vc, slots, hkv, d, bs, nb, k_scale, v_scale, pb, db, flags);
-      break;
+      return cudaLaunchKernelEx(&cfg, reshape_and_cache_kernel<PD_KV_NVFP4>, key, value, kc, vc,
+                                slots, hkv, d, bs, nb, k_scale, v_scale, pb, db, flags);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_absmax(const uint16_t* data, int64_t n, float* out, int num_sms,

@@ -196,16 +196,20 @@ __global__ void __launch_bounds__(kMmaThreads)
     *abort_s = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if constexpr (FMT != PD_KV_NVFP4) {
+    if (tid == kConsumerWarps * 32) {  // the tensor maps are kernel parameters
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
+    }
+  }
   __syncthreads();
+  // Launched as a programmatic dependent of whatever came before on the
+  // stream (the previous step's combine, say): nothing global is read or
+  // written before that grid has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // =========================== producer warp ===============================
   if (warp == kConsumerWarps) {
-    if constexpr (FMT != PD_KV_NVFP4) {
-      if (lane == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
-      }
-    }
     // this CTA's pieces [p_begin, p_end); lane l holds descriptor desc_base + l
     int p_begin = a.plan_cta[blockIdx.x];
     int p_end = a.plan_cta[blockIdx.x + 1];
@@ -648,13 +652,23 @@ cudaError_t launch_bal_cfg(const DecodeArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  // An ordinary launch, not a programmatic dependent: the plan gives every
-  // CTA an equal share on the assumption that all of them start together, and
-  // a CTA launched early next to the previous step's combine grid may find no
-  // room and start a whole share late (measured: 62.6 -> 93 us on the
-  // llama8b batch).
-  kern<<<a.plan_num_ctas, kMmaThreads, smem, st>>>(tk, tv, a);
-  return cudaGetLastError();
+  // A programmatic dependent of the previous work on the stream: the grid is
+  // placed, and its barriers set up, while the previous combine grid drains.
+  // The plan gives every CTA an equal share on the assumption that all of
+  // them start together; that holds because the combine lets its dependents
+  // launch only as its CTAs finish, so no combine CTA still holds the
+  // registers a third partial CTA of an SM needs.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.plan_num_ctas);
+  cfg.blockDim = dim3(kMmaThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, a);
 }
 
 template <int FMT, int D, int NT>

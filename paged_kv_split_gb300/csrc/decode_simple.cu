@@ -176,8 +176,6 @@ __global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
   // Launched as a programmatic dependent of the partial kernel: wait until
   // that grid has completed and its workspace writes are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // and let the next step's partial kernel be scheduled as this grid drains
-  asm volatile("griddepcontrol.launch_dependents;");
   constexpr int kThreads = D / 4;
   const int h = blockIdx.x;
   const int b = blockIdx.y;
@@ -271,6 +269,10 @@ __global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
                         (static_cast<uint32_t>(f32_to_bf16(acc.w * inv)) << 16);
   *reinterpret_cast<uint2*>(a.out + static_cast<int64_t>(b) * a.out_stride + h * D + d) =
       make_uint2(lo01, lo23);
+  // Only now let the next step's partial grid be placed: a combine CTA that
+  // lingered beside it would hold registers that the partial kernel's third
+  // CTA of an SM needs (three balanced BF16 CTAs take 61,440 of the 65,536).
+  asm volatile("griddepcontrol.launch_dependents;");
 }
 
 template <int FMT, int D>
