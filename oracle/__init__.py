@@ -74,6 +74,9 @@ class Oracle:
         L.oracle_decode.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64,
                                     f32, i32, i32, f32, f32]
         L.oracle_decode.restype = ctypes.c_int
+        L.oracle_prefill.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64,
+                                     f32, i32, i32, i32, f32, f32]
+        L.oracle_prefill.restype = ctypes.c_int
         self.lib = L
         self.path = path
 
@@ -155,6 +158,30 @@ class Oracle:
             float(v_scale))
         if rc != 0:
             raise ValueError("oracle_decode: invalid arguments")
+        return out, out_f32
+
+
+    def prefill(self, q, cu_q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads,
+                block_size, num_blocks, scale, causal=True, sliding_window=0, kv_dtype=KV_BF16,
+                k_scale=1.0, v_scale=1.0):
+        """Paged prefill: q uint16 bf16 bits [total_q, Hq, D], cu_q int32 [B+1] query-row
+        offsets. Returns (out bf16 bits [total_q, Hq, D], out before rounding float32)."""
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        cu_q = np.ascontiguousarray(cu_q, dtype=np.int32)
+        block_tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+        seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        T, Hq, D = q.shape
+        B = seq_lens.shape[0]
+        assert cu_q.shape == (B + 1,) and cu_q[-1] == T
+        out = np.empty((T, Hq, D), np.uint16)
+        out_f32 = np.empty((T, Hq, D), np.float32)
+        rc = self.lib.oracle_prefill(
+            _ptr(q), _ptr(cu_q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+            _ptr(seq_lens), _ptr(out), _ptr(out_f32), B, Hq, num_kv_heads, D, block_size,
+            block_tables.shape[1], num_blocks, float(scale), int(bool(causal)),
+            int(sliding_window), kv_dtype, float(k_scale), float(v_scale))
+        if rc != 0:
+            raise ValueError("oracle_prefill: invalid arguments")
         return out, out_f32
 
 

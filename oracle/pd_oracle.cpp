@@ -217,6 +217,53 @@ void read_row(const uint8_t* cache, int kv_dtype, int64_t page, int32_t off, int
   }
 }
 
+/* One query vector qh (q head h, kv head h / group) over keys [lo, hi) of
+ * sequence b, straight from the definition: scores s_j = scale * sum_d
+ * q[d] * k_j[d] (fp32, scale after the dot), two-pass softmax with expf,
+ * out = sum_j e_j v_j (fmaf) / max(sum_j e_j, 1e-20), then bf16. An empty
+ * range gives a zero row. Writes oh (bf16) and, if not null, of (fp32);
+ * returns false for an out-of-range page index. */
+bool attend_one(const uint16_t* qh, int32_t h, int32_t group, int32_t b, int32_t lo, int32_t hi,
+                const uint8_t* k_cache, const uint8_t* v_cache, const int32_t* block_tables,
+                int32_t max_blocks_per_seq, int64_t num_blocks, int32_t num_kv_heads,
+                int32_t head_dim, int32_t block_size, float scale, int32_t kv_dtype,
+                float k_scale, float v_scale, uint16_t* oh, float* of) {
+  const int32_t g = h / group;
+  const int32_t n = hi > lo ? hi - lo : 0;
+  std::vector<float> krow(head_dim), vrow(head_dim), acc(head_dim, 0.0f), s(n);
+  for (int32_t j = lo; j < hi; ++j) {
+    const int64_t page = block_tables[static_cast<int64_t>(b) * max_blocks_per_seq + j / block_size];
+    if (page < 0 || page >= num_blocks) return false;
+    read_row(k_cache, kv_dtype, page, j % block_size, g, block_size, num_kv_heads, head_dim,
+             k_scale, krow.data());
+    float dot = 0.0f;
+    for (int32_t i = 0; i < head_dim; ++i) dot = dot + bf16_value(qh[i]) * krow[i];
+    s[j - lo] = scale * dot;
+  }
+  float m = -std::numeric_limits<float>::infinity();
+  for (int32_t j = 0; j < n; ++j)
+    if (s[j] > m) m = s[j];
+  float l = 0.0f;
+  for (int32_t j = 0; j < n; ++j) {
+    s[j] = std::exp(s[j] - m);
+    l = l + s[j];
+  }
+  for (int32_t j = lo; j < hi; ++j) {
+    const int64_t page = block_tables[static_cast<int64_t>(b) * max_blocks_per_seq + j / block_size];
+    read_row(v_cache, kv_dtype, page, j % block_size, g, block_size, num_kv_heads, head_dim,
+             v_scale, vrow.data());
+    const float e = s[j - lo];
+    for (int32_t i = 0; i < head_dim; ++i) acc[i] = std::fmaf(e, vrow[i], acc[i]);
+  }
+  const float denom = l > 1e-20f ? l : 1e-20f;
+  for (int32_t i = 0; i < head_dim; ++i) {
+    const float o = acc[i] / denom;
+    oh[i] = bf16_round(o);
+    if (of) of[i] = o;
+  }
+  return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -329,57 +376,66 @@ int oracle_decode(const uint16_t* q, const uint8_t* k_cache, const uint8_t* v_ca
   if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return -1;
   if (kv_dtype == KV_NVFP4 && head_dim % 16 != 0) return -1;
   const int32_t group = num_q_heads / num_kv_heads;
-  std::vector<float> krow(head_dim), vrow(head_dim), acc(head_dim);
   for (int32_t b = 0; b < num_seqs; ++b) {
     const int32_t len = seq_lens[b];
     if (len < 0 || static_cast<int64_t>(len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
       return -1;
     const int32_t lo = (sliding_window > 0 && len > sliding_window) ? len - sliding_window : 0;
     for (int32_t h = 0; h < num_q_heads; ++h) {
-      const int32_t g = h / group;
-      const uint16_t* qh = q + (static_cast<int64_t>(b) * num_q_heads + h) * head_dim;
-      uint16_t* oh = out + (static_cast<int64_t>(b) * num_q_heads + h) * head_dim;
-      float* of = out_f32 ? out_f32 + (static_cast<int64_t>(b) * num_q_heads + h) * head_dim
-                          : nullptr;
-      const int32_t n = len - lo;
-      if (n <= 0) {
-        for (int32_t i = 0; i < head_dim; ++i) {
-          oh[i] = bf16_round(0.0f);
-          if (of) of[i] = 0.0f;
-        }
-        continue;
-      }
-      std::vector<float> s(n);
-      for (int32_t j = lo; j < len; ++j) {
-        const int64_t page = block_tables[static_cast<int64_t>(b) * max_blocks_per_seq + j / block_size];
-        if (page < 0 || page >= num_blocks) return -1;
-        read_row(k_cache, kv_dtype, page, j % block_size, g, block_size, num_kv_heads, head_dim,
-                 k_scale, krow.data());
-        float dot = 0.0f;
-        for (int32_t i = 0; i < head_dim; ++i) dot = dot + bf16_value(qh[i]) * krow[i];
-        s[j - lo] = scale * dot;
-      }
-      float m = -std::numeric_limits<float>::infinity();
-      for (int32_t j = 0; j < n; ++j)
-        if (s[j] > m) m = s[j];
-      float l = 0.0f;
-      for (int32_t j = 0; j < n; ++j) {
-        s[j] = std::exp(s[j] - m);
-        l = l + s[j];
-      }
-      for (int32_t i = 0; i < head_dim; ++i) acc[i] = 0.0f;
-      for (int32_t j = lo; j < len; ++j) {
-        const int64_t page = block_tables[static_cast<int64_t>(b) * max_blocks_per_seq + j / block_size];
-        read_row(v_cache, kv_dtype, page, j % block_size, g, block_size, num_kv_heads, head_dim,
-                 v_scale, vrow.data());
-        const float e = s[j - lo];
-        for (int32_t i = 0; i < head_dim; ++i) acc[i] = std::fmaf(e, vrow[i], acc[i]);
-      }
-      const float denom = l > 1e-20f ? l : 1e-20f;
-      for (int32_t i = 0; i < head_dim; ++i) {
-        const float o = acc[i] / denom;
-        oh[i] = bf16_round(o);
-        if (of) of[i] = o;
+      const int64_t row = static_cast<int64_t>(b) * num_q_heads + h;
+      if (!attend_one(q + row * head_dim, h, group, b, lo, len, k_cache, v_cache, block_tables,
+                      max_blocks_per_seq, num_blocks, num_kv_heads, head_dim, block_size, scale,
+                      kv_dtype, k_scale, v_scale, out + row * head_dim,
+                      out_f32 ? out_f32 + row * head_dim : nullptr))
+        return -1;
+    }
+  }
+  return 0;
+}
+
+/* Paged prefill (chunked prefill) attention over the same caches: several
+ * query tokens per sequence. The pages name this unit beside decode
+ * (pegainfer issue 1008: `prefill_paged_launch` over the paged-KV view;
+ * AstrAI "csrc/tests" log: prefill kernels templated on the paged KV source,
+ * one `causal_offset` with -1 = off and >= 0 = the first query position,
+ * stride addressing for Q/KV/O). Sequence b owns query rows
+ * [cu_q[b], cu_q[b+1]) of q and out (bf16 [total_q, num_q_heads, head_dim])
+ * and L_b = seq_lens[b] keys in the cache, its new tokens included, so
+ * q_len_b <= L_b. causal != 0: the queries are the sequence's newest tokens,
+ * query i at position p = L_b - q_len_b + i, and it sees keys j <= p (the
+ * first query position of sequence b is L_b - q_len_b). causal == 0: every
+ * query sees all L_b keys, p = L_b - 1. A window W > 0 keeps keys j with
+ * p - j < W. Each (query, head) is then the decode definition above over
+ * keys [lo, p + 1): fp32 dot, scale after the dot, two-pass softmax with
+ * expf, fmaf accumulation of V, 1e-20 guard, bf16 round to nearest even.
+ * Returns 0, or -1 for a bad shape or an out-of-range page index. */
+int oracle_prefill(const uint16_t* q, const int32_t* cu_q, const uint8_t* k_cache,
+                   const uint8_t* v_cache, const int32_t* block_tables, const int32_t* seq_lens,
+                   uint16_t* out, float* out_f32, int32_t num_seqs, int32_t num_q_heads,
+                   int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                   int32_t max_blocks_per_seq, int64_t num_blocks, float scale, int32_t causal,
+                   int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale) {
+  if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return -1;
+  if (kv_dtype == KV_NVFP4 && head_dim % 16 != 0) return -1;
+  const int32_t group = num_q_heads / num_kv_heads;
+  for (int32_t b = 0; b < num_seqs; ++b) {
+    const int32_t len = seq_lens[b];
+    const int32_t q_len = cu_q[b + 1] - cu_q[b];
+    if (len < 0 || q_len < 0 || q_len > len ||
+        static_cast<int64_t>(len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
+      return -1;
+    for (int32_t i = 0; i < q_len; ++i) {
+      const int64_t qrow = static_cast<int64_t>(cu_q[b]) + i;
+      const int32_t pos = causal ? len - q_len + i : len - 1;  // the query's position
+      const int32_t hi = pos + 1;                               // keys [lo, hi)
+      const int32_t lo = (sliding_window > 0 && hi > sliding_window) ? hi - sliding_window : 0;
+      for (int32_t h = 0; h < num_q_heads; ++h) {
+        const int64_t row = qrow * num_q_heads + h;
+        if (!attend_one(q + row * head_dim, h, group, b, lo, hi, k_cache, v_cache, block_tables,
+                        max_blocks_per_seq, num_blocks, num_kv_heads, head_dim, block_size, scale,
+                        kv_dtype, k_scale, v_scale, out + row * head_dim,
+                        out_f32 ? out_f32 + row * head_dim : nullptr))
+          return -1;
       }
     }
   }

@@ -241,3 +241,34 @@ def quantised(kv_dtype: int, seed: int = 0, num_seqs: int = 64, lo: int = 512,
     tag = {1: "fp8", 2: "nvfp4"}[kv_dtype]
     return make_case(f"quant_{tag}_b{num_seqs}", lens, 64, 8, 128, 16, seed=seed,
                      kv_dtype=kv_dtype)
+
+
+def make_prefill_case(name, seq_lens, q_lens, num_q_heads, num_kv_heads, head_dim, block_size,
+                      *, seed=0, sliding_window=0, extra_blocks=0, q_std=1.0,
+                      kv_std=1.0) -> Case:
+    """A chunked-prefill workload over the same paged cache: every token of
+    every sequence is in the cache (as in make_case), and sequence b has
+    q_lens[b] query rows, its newest tokens. q becomes [sum(q_lens), Hq, D];
+    extra["cu_q"] holds the row offsets [B+1] and extra["q_lens"] the lengths."""
+    case = make_case(name, seq_lens, num_q_heads, num_kv_heads, head_dim, block_size, seed=seed,
+                     sliding_window=sliding_window, extra_blocks=extra_blocks, q_std=q_std,
+                     kv_std=kv_std)
+    q_lens = np.asarray(q_lens, dtype=np.int32)
+    assert q_lens.shape == (case.num_seqs,) and np.all(q_lens <= case.seq_lens)
+    cu_q = np.zeros(case.num_seqs + 1, np.int32)
+    cu_q[1:] = np.cumsum(q_lens)
+    case.q = normal_bf16(seed + 6, (int(cu_q[-1]), num_q_heads, head_dim), q_std)
+    case.extra["cu_q"] = cu_q
+    case.extra["q_lens"] = q_lens
+    return case
+
+
+def prefill_chunked(seed: int = 0, num_seqs: int = 8, chunk: int = 512,
+                    max_context: int = 3584) -> Case:
+    """Chunked prefill at Llama-3-8B shapes (32 q / 8 kv heads, D=128, bs=16):
+    each of num_seqs sequences adds a chunk of `chunk` tokens after a context
+    of U[0, max_context] tokens already in the cache."""
+    ctx = uniform_int(seed + 5, num_seqs, 0, max_context)
+    lens = ctx + chunk
+    return make_prefill_case(f"prefill_b{num_seqs}_c{chunk}", lens, np.full(num_seqs, chunk),
+                             32, 8, 128, 16, seed=seed)

@@ -130,3 +130,36 @@ def sdpa_f64(q_bits: np.ndarray, kpages: np.ndarray, vpages: np.ndarray, block_t
         o = torch.nn.functional.scaled_dot_product_attention(qt, Kt, Vt, scale=float(scale))
         out[b] = o[:, 0, :].numpy()
     return out
+
+
+def prefill_f64(q_bits: np.ndarray, cu_q, kpages: np.ndarray, vpages: np.ndarray, block_tables,
+                seq_lens, scale: float, causal: bool = True,
+                sliding_window: int = 0) -> np.ndarray:
+    """Reference paged prefill in float64: per sequence, one [q_len, Hq, L]
+    score tensor with the causal / window mask, a masked softmax and one
+    contraction with V (numpy einsum; no loop over keys)."""
+    T, Hq, D = q_bits.shape
+    hkv = kpages.shape[2]
+    g = Hq // hkv
+    q = bf16_to_f64(q_bits)
+    out = np.zeros((T, Hq, D))
+    for b in range(len(seq_lens)):
+        L = int(seq_lens[b])
+        r0, r1 = int(cu_q[b]), int(cu_q[b + 1])
+        ql = r1 - r0
+        if ql == 0:
+            continue
+        K = np.repeat(gather_sequence(kpages, block_tables[b], L), g, axis=1)  # [L, Hq, D]
+        V = np.repeat(gather_sequence(vpages, block_tables[b], L), g, axis=1)
+        pos = (L - ql + np.arange(ql)) if causal else np.full(ql, L - 1)
+        j = np.arange(L)
+        keep = j[None, :] <= pos[:, None]
+        if sliding_window > 0:
+            keep &= (pos[:, None] - j[None, :]) < sliding_window
+        s = np.einsum("qhd,lhd->qhl", q[r0:r1], K) * float(scale)
+        s = np.where(keep[:, None, :], s, -np.inf)
+        s = s - s.max(axis=-1, keepdims=True)
+        e = np.exp(s)
+        e = e / e.sum(axis=-1, keepdims=True)
+        out[r0:r1] = np.einsum("qhl,lhd->qhd", e, V)
+    return out

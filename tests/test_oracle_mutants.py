@@ -21,11 +21,18 @@ def _sdpa_all(orc):
             TD.test_oracle_matches_sdpa_f64(orc, kv, i)
 
 
+def _prefill_all(orc):
+    from tests import test_oracle_prefill as TP
+    for idx in range(len(TP.PREFILL_CASES)):
+        for causal in (True, False):
+            TP.test_prefill_matches_f64(orc, idx, 0, causal)
+
+
 MUTANTS = [
     ("gqa kv head index", "const int32_t g = h / group;", "const int32_t g = h % num_kv_heads;",
      [_sdpa_all]),
-    ("window start off by one", "len - sliding_window : 0", "len - sliding_window + 1 : 0",
-     [_sdpa_all]),
+    ("window start off by one", "len > sliding_window) ? len - sliding_window : 0",
+     "len > sliding_window) ? len - sliding_window + 1 : 0", [_sdpa_all]),
     ("score scale dropped", "s[j - lo] = scale * dot;", "s[j - lo] = dot;", [_sdpa_all]),
     ("softmax max not subtracted", "s[j] = std::exp(s[j] - m);", "s[j] = std::exp(s[j]);",
      [lambda o: [TD.test_large_scores_stay_finite(o, k) for k in (0, 1, 2)]]),
@@ -53,6 +60,14 @@ MUTANTS = [
      [TC.test_nvfp4_cache_matches_definition]),
     ("fp8 calibration divisor", "amax / 448.0f : 1.0f", "amax / 240.0f : 1.0f",
      [TX.test_fp8_scale_is_absmax_over_448]),
+    ("prefill causal bound excludes the query's own key", "const int32_t hi = pos + 1;",
+     "const int32_t hi = pos;", [_prefill_all]),
+    ("prefill first query position", "causal ? len - q_len + i : len - 1;",
+     "causal ? len - q_len + i - 1 : len - 1;", [_prefill_all]),
+    ("prefill window measured from the last key", "hi > sliding_window) ? hi - sliding_window",
+     "len > sliding_window) ? len - sliding_window", [_prefill_all]),
+    ("prefill q row offset", "const int64_t qrow = static_cast<int64_t>(cu_q[b]) + i;",
+     "const int64_t qrow = static_cast<int64_t>(cu_q[b]) + i / 2;", [_prefill_all]),
     ("fp8 quantise multiplies", "return std::isnan(x) ? x : x / s;",
      "return std::isnan(x) ? x : x * s;", [TC.test_fp8_cache_matches_torch_e4m3]),
 ]
