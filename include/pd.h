@@ -356,6 +356,40 @@ int pd_decode_static_ws(const void* q, const void* k_cache, const void* v_cache,
                         int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
                         void* stream);
 
+/* Paged prefill (chunked prefill) attention over the same paged cache:
+ * several query tokens per sequence. pegainfer issue 1008 names the unit
+ * (`prefill_paged_launch` over the paged-KV view); the AstrAI "csrc/tests"
+ * log gives its interface: one causal offset (-1 = off, >= 0 = the first
+ * query position), stride addressing for Q and O, the paged KV source.
+ *   q, out      bf16; query row i (i in [0, cu_q[num_seqs])) holds the
+ *               num_q_heads x head_dim values of one token at element
+ *               i * q_stride / i * out_stride (0 = packed, num_q_heads *
+ *               head_dim; otherwise at least that and a multiple of 8).
+ *   cu_q        int32 [num_seqs + 1], device: sequence b owns query rows
+ *               [cu_q[b], cu_q[b+1]), its q_len_b newest tokens.
+ *   seq_lens    int32 [num_seqs], device: L_b keys in the cache, the new
+ *               tokens already written (pd_reshape_and_cache), q_len_b <= L_b.
+ *   max_q_len   host int: the largest q_len_b; the grid covers that many
+ *               tokens per sequence (a longer one raises PD_DEV_BAD_SEQ_LEN).
+ *   causal      != 0: query i of sequence b sits at position L_b - q_len_b + i
+ *               (the causal offset of the sequence is L_b - q_len_b) and sees
+ *               keys j <= its position; 0: every query sees all L_b keys.
+ *   sliding_window  W > 0 keeps keys j with position - j < W; 0 = off.
+ * Scores, softmax and the bf16 output follow pd_decode (scale after the dot
+ * product, 1e-20 guard). Cache, block tables, scale, status codes and device
+ * flags as in pd_decode. Supported: kv_dtype PD_KV_BF16, head_dim 64 or 128,
+ * block_size 16 or 32, G = num_q_heads / num_kv_heads <= 16; anything else
+ * returns PD_ERR_UNSUPPORTED. No workspace: each query tile writes its rows.
+ * Device pointers owned by the caller, 16-byte aligned; enqueued on `stream`,
+ * never synchronises. */
+int pd_prefill(const void* q, int64_t q_stride, const int32_t* cu_q, const void* k_cache,
+               const void* v_cache, const int32_t* block_tables, const int32_t* seq_lens,
+               void* out, int64_t out_stride, int32_t num_seqs, int32_t max_q_len,
+               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+               int32_t max_blocks_per_seq, int64_t num_blocks, float scale, int32_t causal,
+               int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
+               void* stream);
+
 /* Read (and, if reset != 0, clear) the pd_device_flag bits that kernels on
  * the current device have raised since the last reset. Synchronises the
  * device (cudaMemcpyFromSymbol): a debugging call, not for the hot path. */

@@ -56,6 +56,9 @@ _lib.pd_decode_partial.restype = ctypes.c_int
 _lib.pd_decode_combine.argtypes = [_P, _sz, _P, _P, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _P]
 _lib.pd_decode_combine.restype = ctypes.c_int
 _lib.pd_device_status.argtypes, _lib.pd_device_status.restype = [_P, _i32], ctypes.c_int
+_lib.pd_prefill.argtypes = [_P, _i64, _P, _P, _P, _P, _P, _P, _i64, _i32, _i32, _i32, _i32, _i32,
+                            _i32, _i32, _i64, _f32, _i32, _i32, _i32, _f32, _f32, _P]
+_lib.pd_prefill.restype = ctypes.c_int
 _lib.pd_prefer_balanced.argtypes = [_P, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]
 _lib.pd_prefer_balanced.restype = ctypes.c_int
 _lib.pd_balanced_plan_bytes.argtypes = [_i32, _i32, _i32]
@@ -454,4 +457,59 @@ def pd_decode_balanced_strided(q_rows, k_cache, v_cache, block_tables, plan_dev,
         _dev(workspace, "workspace", None, dev), workspace.numel() * workspace.element_size(),
         _stream(stream))
     _check("pd_decode_balanced_strided", rc)
+    return out_rows
+
+
+# ---- paged prefill ---------------------------------------------------------
+def pd_prefill(q, cu_q, k_cache, v_cache, block_tables, seq_lens, out, *, max_q_len,
+               num_kv_heads, block_size, num_blocks, scale, causal=True, sliding_window=0,
+               kv_dtype=PD_KV_BF16, k_scale=1.0, v_scale=1.0, stream=None):
+    """Paged (chunked) prefill. q and out: contiguous bf16 [total_q, Hq, D];
+    cu_q: int32 [B + 1] query-row offsets; seq_lens: int32 [B] keys in the
+    cache (new tokens included); max_q_len: host int, the largest q length.
+    pd_prefill_strided takes token rows of a wider buffer instead."""
+    if q.dim() != 3 or out.dim() != 3:
+        raise ValueError("q and out must be bf16 [total_q, num_q_heads, head_dim]")
+    T, hq, d = q.shape
+    if tuple(out.shape) != (T, hq, d):
+        raise ValueError("out must have q's shape")
+    B = int(seq_lens.shape[0])
+    if tuple(cu_q.shape) != (B + 1,):
+        raise ValueError("cu_q must be int32 [num_seqs + 1]")
+    dev = q.device
+    rc = _lib.pd_prefill(
+        _dev(q, "q", torch.bfloat16, dev), 0, _dev(cu_q, "cu_q", torch.int32, dev),
+        _dev(k_cache, "k_cache", None, dev), _dev(v_cache, "v_cache", None, dev),
+        _dev(block_tables, "block_tables", torch.int32, dev),
+        _dev(seq_lens, "seq_lens", torch.int32, dev), _dev(out, "out", torch.bfloat16, dev), 0,
+        B, int(max_q_len), hq, num_kv_heads, d, block_size, block_tables.shape[1], num_blocks,
+        float(scale), int(bool(causal)), int(sliding_window), _dtype_code(kv_dtype),
+        float(k_scale), float(v_scale), _stream(stream))
+    _check("pd_prefill", rc)
+    return out
+
+
+def pd_prefill_strided(q_rows, cu_q, k_cache, v_cache, block_tables, seq_lens, out_rows, *,
+                       num_q_heads, head_dim, max_q_len, num_kv_heads, block_size, num_blocks,
+                       scale, causal=True, sliding_window=0, kv_dtype=PD_KV_BF16, k_scale=1.0,
+                       v_scale=1.0, stream=None):
+    """pd_prefill with token rows of a wider buffer: q_rows / out_rows are
+    contiguous bf16 [total_q, row] tensors holding each token's Hq * D
+    values in the first Hq * D of its row (fused QKV rows, padded outputs)."""
+    T, stride = _strided_rows(q_rows, num_q_heads, head_dim, "q_rows")
+    To, ostride = _strided_rows(out_rows, num_q_heads, head_dim, "out_rows")
+    if To != T:
+        raise ValueError("q_rows and out_rows have different numbers of rows")
+    B = int(seq_lens.shape[0])
+    dev = q_rows.device
+    rc = _lib.pd_prefill(
+        _dev(q_rows, "q_rows", torch.bfloat16, dev), stride, _dev(cu_q, "cu_q", torch.int32, dev),
+        _dev(k_cache, "k_cache", None, dev), _dev(v_cache, "v_cache", None, dev),
+        _dev(block_tables, "block_tables", torch.int32, dev),
+        _dev(seq_lens, "seq_lens", torch.int32, dev),
+        _dev(out_rows, "out_rows", torch.bfloat16, dev), ostride, B, int(max_q_len),
+        num_q_heads, num_kv_heads, head_dim, block_size, block_tables.shape[1], num_blocks,
+        float(scale), int(bool(causal)), int(sliding_window), _dtype_code(kv_dtype),
+        float(k_scale), float(v_scale), _stream(stream))
+    _check("pd_prefill_strided", rc)
     return out_rows

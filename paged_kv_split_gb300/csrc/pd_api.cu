@@ -814,6 +814,60 @@ int pd_decode_balanced_combine(const void* q, const void* k_cache, const void* v
                          num_pieces, workspace, workspace_bytes, stream, false, true);
 }
 
+int pd_prefill(const void* q, int64_t q_stride, const int32_t* cu_q, const void* k_cache,
+               const void* v_cache, const int32_t* block_tables, const int32_t* seq_lens,
+               void* out, int64_t out_stride, int32_t num_seqs, int32_t max_q_len,
+               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+               int32_t max_blocks_per_seq, int64_t num_blocks, float scale, int32_t causal,
+               int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
+               void* stream) {
+  (void)k_scale;
+  (void)v_scale;
+  if (num_seqs < 0 || num_seqs > 65535 || max_q_len < 0) return PD_ERR_INVALID_ARG;
+  if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return PD_ERR_INVALID_ARG;
+  const int G = num_q_heads / num_kv_heads;
+  if (G > kMaxGroup || num_kv_heads > 65535) return PD_ERR_UNSUPPORTED;
+  if (!dtype_ok(kv_dtype) || !head_dim_ok(head_dim) || !block_size_ok(block_size))
+    return PD_ERR_UNSUPPORTED;
+  if (kv_dtype != PD_KV_BF16 || head_dim > 128) return PD_ERR_UNSUPPORTED;
+  if (max_blocks_per_seq <= 0 || num_blocks <= 0 || sliding_window < 0) return PD_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(max_blocks_per_seq) * block_size > (int64_t{1} << 30))
+    return PD_ERR_INVALID_ARG;
+  if (num_blocks * block_size > INT32_MAX) return PD_ERR_INVALID_ARG;
+  if (!q_stride_ok(q_stride, num_q_heads, head_dim) || !q_stride_ok(out_stride, num_q_heads, head_dim))
+    return PD_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return PD_ERR_INVALID_ARG;
+  if (num_seqs == 0 || max_q_len == 0) return PD_OK;
+  if (!dev_ptr_ok(q) || !dev_ptr_ok(cu_q) || !dev_ptr_ok(k_cache) || !dev_ptr_ok(v_cache) ||
+      !dev_ptr_ok(block_tables) || !dev_ptr_ok(seq_lens) || !dev_ptr_ok(out))
+    return PD_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if (current_device(&dev) != cudaSuccess) return PD_ERR_CUDA;
+  PrefillArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.q_stride = q_stride ? q_stride : static_cast<int64_t>(num_q_heads) * head_dim;
+  a.cu_q = cu_q;
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.out = static_cast<uint16_t*>(out);
+  a.out_stride = out_stride ? out_stride : static_cast<int64_t>(num_q_heads) * head_dim;
+  a.flags = dev->flags;
+  a.num_blocks = num_blocks;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.group = G;
+  a.block_size = block_size;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.tokens_per_cta = 64 / G;
+  a.causal = causal != 0;
+  a.sliding_window = sliding_window;
+  a.scale_log2 = scale * kLog2e;
+  return cuda_status(launch_prefill(a, k_cache, v_cache, head_dim, max_q_len,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
 int pd_device_status(int32_t* flags, int32_t reset) {
   if (flags == nullptr) return PD_ERR_INVALID_ARG;
   DeviceInfo* dev = nullptr;

@@ -179,6 +179,24 @@ struct CombineArgs {
   int num_kv_heads;
 };
 
+// Paged prefill: sequence b's query rows are cu_q[b] .. cu_q[b+1]-1 of q and
+// out (row r at r * q_stride / r * out_stride elements, Hq * D values each).
+struct PrefillArgs {
+  const uint16_t* q;
+  int64_t q_stride;
+  const int32_t* cu_q;           // [B + 1]
+  const int32_t* block_tables;   // [B][MBS]
+  const int32_t* seq_lens;       // [B], keys in the cache, the new tokens included
+  uint16_t* out;
+  int64_t out_stride;
+  int* flags;
+  int64_t num_blocks;
+  int num_seqs, num_q_heads, num_kv_heads, group, block_size, max_blocks_per_seq;
+  int tokens_per_cta;            // query tokens of one CTA: 64 / group
+  int causal, sliding_window;
+  float scale_log2;              // scale * log2(e)
+};
+
 // Sequence length as the kernels use it: clamped to the block table, with a
 // flag raised for values outside [0, MBS*bs].
 __device__ __forceinline__ int checked_seq_len(const int32_t* seq_lens, int b, int mbs, int bs,
@@ -214,4 +232,7 @@ cudaError_t launch_decode_partial_balanced(const DecodeArgs& a, int head_dim, in
 // Resident CTAs per SM of the balanced partial kernel for a GQA group size.
 int balanced_ctas_per_sm(int kv_dtype, int head_dim, int group);
 cudaError_t launch_decode_combine(const CombineArgs& a, int head_dim, cudaStream_t st);
+// Paged prefill over a BF16 cache (head_dim 64 / 128); grid.x = q tiles.
+cudaError_t launch_prefill(const PrefillArgs& a, const void* k_cache, const void* v_cache,
+                           int head_dim, int max_q_len, cudaStream_t st);
 }  // namespace pd

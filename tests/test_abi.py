@@ -158,3 +158,37 @@ def test_reshape_and_cache_validation(pdlib):
     assert call(kc=0x3001) == 1
     assert call(dt=1, ks=-1.0) == 1
     assert call(nb=0) == 1
+
+
+def test_prefill_validation(pdlib):
+    """pd_prefill refuses bad shapes on the host; the pointers are never touched."""
+    _, L = pdlib
+    f = L.pd_prefill
+    P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    f.argtypes = [P, i64, P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, i32, i32, i64, f32,
+                  i32, i32, i32, f32, f32, P]
+    ok = dict(q=0x1000, qs=0, cu=0x2000, kc=0x3000, vc=0x4000, bt=0x5000, sl=0x6000, o=0x7000,
+              os=0, B=2, mq=16, Hq=8, Hkv=2, D=128, bs=16, mbs=8, nb=32, sc=0.088, causal=1, W=0,
+              dt=0, ks=1.0, vs=1.0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["q"], a["qs"], a["cu"], a["kc"], a["vc"], a["bt"], a["sl"], a["o"], a["os"],
+                 a["B"], a["mq"], a["Hq"], a["Hkv"], a["D"], a["bs"], a["mbs"], a["nb"], a["sc"],
+                 a["causal"], a["W"], a["dt"], a["ks"], a["vs"], None)
+    assert call(B=0) == 0                 # nothing to do, no launch
+    assert call(mq=0) == 0
+    assert call(dt=1) == 2                # FP8 / NVFP4 caches: not built for prefill
+    assert call(dt=2) == 2
+    assert call(D=256) == 2               # head_dim above 128: not built for prefill
+    assert call(D=96) == 2
+    assert call(bs=8) == 2
+    assert call(Hq=34, Hkv=2) == 2        # group of 17 > 16
+    assert call(Hq=6, Hkv=4) == 1         # GQA ratio not integral
+    assert call(mq=-1) == 1
+    assert call(W=-1) == 1
+    assert call(qs=100) == 1              # stride shorter than a token's heads
+    assert call(os=1028) == 1             # stride not a multiple of 8 elements
+    assert call(q=0x1004) == 1            # misaligned pointer
+    assert call(cu=0) == 1                # null pointer
+    assert call(sc=float("inf")) == 1
