@@ -13,6 +13,10 @@ the same through the C ABI from pinned host inputs, planning included.
                     [--workload llama8b|long_b4_32k|...] [--splits S]
                     [--schedule auto|split|balanced]
 
+The prefill_* workloads time pd_prefill (paged chunked prefill over the same
+cache) instead: value = attention TFLOP/s (4 * head_dim per query row, q head
+and key seen), roofline against the measured bf16 tensor peak.
+
 With torchrun (N > 1) every rank decodes its own independent batch (seeded by
 rank, replicas only: no data is exchanged); the barrier and max-over-ranks
 timing use torch.distributed.
@@ -60,8 +64,32 @@ def workload(name: str, rank: int = 0):
         # the llama8b batch with quantised caches (same shapes, same lengths)
         "llama8b_fp8": lambda: _with_dtype(I.llama8b(seed=seed), 1),
         "llama8b_nvfp4": lambda: _with_dtype(I.llama8b(seed=seed), 2),
+        # paged (chunked) prefill over the same BF16 cache (pd_prefill)
+        "prefill_chunked": lambda: I.prefill_chunked(seed=seed),
+        "prefill_long": lambda: I.prefill_chunked(seed=seed, num_seqs=16, chunk=256,
+                                                  max_context=7936),
     }
     return table[name]()
+
+
+PREFILL_METRIC = "prefill µs/step and attention TFLOP/s (% of GB300 bf16 peak) at 1 GPU"
+
+
+def prefill_flops(case, rows=None) -> float:
+    """4 * D per (query row, q head, key seen): the two contractions Q K^T and
+    P V, causal (query i of a sequence sees L - q_len + i + 1 keys), within the
+    window. rows: optional (sequence, first row, last row + 1) sample."""
+    cu = case.extra["cu_q"]
+    W = case.sliding_window
+    total = 0
+    spans = rows or [(b, 0, int(cu[b + 1] - cu[b])) for b in range(case.num_seqs)]
+    for b, i0, i1 in spans:
+        L, ql = int(case.seq_lens[b]), int(cu[b + 1] - cu[b])
+        seen = L - ql + np.arange(i0, i1, dtype=np.int64) + 1
+        if W > 0:
+            seen = np.minimum(seen, W)
+        total += int(seen.sum())
+    return 4.0 * case.head_dim * case.num_q_heads * total
 
 
 def _with_dtype(case, kv_dtype):
@@ -588,11 +616,209 @@ def run_pd(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def time_oracle_prefill(case, kc_host, vc_host, budget_s: float):
+    """oracle_prefill as it stands, single-threaded, on a bounded sample: the
+    last k query rows of the first sequence, k grown until a call takes about
+    budget_s; median of three calls."""
+    import oracle
+    orc = oracle.get()
+    ql = int(case.extra["cu_q"][1])
+
+    def call(k):
+        t = time.perf_counter()
+        orc.prefill(case.q[ql - k:ql], np.array([0, k], np.int32), kc_host, vc_host,
+                    case.block_tables[:1], case.seq_lens[:1], case.num_kv_heads,
+                    case.block_size, case.num_blocks, case.scale, True, case.sliding_window)
+        return time.perf_counter() - t
+    k = 1
+    while True:
+        dt = call(k)
+        if dt >= budget_s or k >= ql:
+            break
+        k = min(ql, max(k + 1, int(k * budget_s / max(dt, 1e-3))))
+    dt = statistics.median([dt, call(k), call(k)])
+    flops = prefill_flops(case, [(0, ql - k, ql)])
+    return k, dt, flops
+
+
+def run_prefill(args, rank, world, local):
+    import torch
+    from paged_kv_split_gb300 import binding as pd
+
+    dev = torch.device("cuda", local if world > 1 else 0)
+    case = workload(args.workload, rank)
+    T, hq, D = case.q.shape
+    cu = case.extra["cu_q"]
+    max_q = int(case.extra["q_lens"].max())
+    flops = prefill_flops(case)
+    page_bytes = pd.pd_page_bytes(0, case.block_size, case.num_kv_heads, D)
+    cache_bytes = case.num_blocks * page_bytes
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    replicas = max(2, math.ceil(3 * l2 / max(2 * cache_bytes, 1)))
+    caches, _, _ = build_device_state(case, 0, replicas, dev)
+    q = torch.from_numpy(case.q.view(np.int16)).to(dev).view(torch.bfloat16)
+    out = torch.empty_like(q)
+    cu_d = torch.from_numpy(cu).to(dev)
+    bt = torch.from_numpy(case.block_tables).to(dev)
+    lens = torch.from_numpy(case.seq_lens).to(dev)
+    kw = dict(max_q_len=max_q, num_kv_heads=case.num_kv_heads, block_size=case.block_size,
+              num_blocks=case.num_blocks, scale=case.scale, causal=True,
+              sliding_window=case.sliding_window)
+
+    def step(i):
+        kc, vc = caches[i % replicas]
+        pd.pd_prefill(q, cu_d, kc, vc, bt, lens, out, **kw)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    time.sleep(0.3)  # first samples before the timed region
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    ms_local = e0.elapsed_time(e1) / args.steps
+    ms_step = max_over_ranks(ms_local, world)
+    total_flops = sum_over_ranks(flops, world)
+    tflops = total_flops / (ms_step * 1e-3) / 1e12
+    clocks = sampler.summary(t0, t1)
+    sampler.stop()
+
+    # e2e through the C ABI: q, cu_q and lengths from pinned host memory, the
+    # output read back, every step
+    q_h = torch.from_numpy(case.q.view(np.int16)).pin_memory()
+    cu_h = torch.from_numpy(cu).pin_memory()
+    lens_h = torch.from_numpy(case.seq_lens).pin_memory()
+    out_h = torch.empty(q_h.shape, dtype=torch.int16).pin_memory()
+    q_e = torch.empty_like(q)
+    cu_e, lens_e = torch.empty_like(cu_d), torch.empty_like(lens)
+
+    def e2e_step(i):
+        q_e.view(torch.int16).copy_(q_h, non_blocking=True)
+        cu_e.copy_(cu_h, non_blocking=True)
+        lens_e.copy_(lens_h, non_blocking=True)
+        kc, vc = caches[i % replicas]
+        pd.pd_prefill(q_e, cu_e, kc, vc, bt, lens_e, out, **kw)
+        out_h.copy_(out.view(torch.int16), non_blocking=True)
+
+    n_e2e = max(3, min(args.steps, 200))
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(n_e2e):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world)
+    h2d = q_h.numel() * 2 + cu_h.numel() * 4 + lens_h.numel() * 4
+    d2h = out_h.numel() * 2
+    if rank != 0:
+        return
+    peak_t = None
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            peak_t, peak_src = float(json.load(f)["bf16_tflops"]), "measured (bf16 burst)"
+    if peak_t is None:
+        peak_t, peak_src = 1900.0, "fallback"
+    achieved = flops / (ms_local * 1e-3) / 1e12
+    line = {
+        "metric": PREFILL_METRIC, "value": round(tflops, 1), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "us_per_step": round(ms_step * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "num_seqs": case.num_seqs, "query_rows": T,
+                   "num_q_heads": hq, "num_kv_heads": case.num_kv_heads, "head_dim": D,
+                   "block_size": case.block_size, "kv_dtype": "bf16", "causal": True,
+                   "max_q_len": max_q, "keys_max": int(case.seq_lens.max()),
+                   "flops_per_step": flops,
+                   "l2": f"inputs larger than L2: {replicas} cache replicas of "
+                         f"{2 * cache_bytes / 1e6:.0f} MB rotated per step "
+                         f"(L2 {l2 / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "prefill_mma_kernel (mma.sync bf16)",
+                     "achieved": round(achieved, 1), "peak": peak_t, "peak_source": peak_src,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak_t, 4), "traffic": None},
+        "e2e": {"value": round(total_flops / (ms_e2e * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+                "us_per_step": round(ms_e2e * 1e3, 1), "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        kc, vc = caches[0]
+        k, dt, sflops = time_oracle_prefill(case, kc.cpu().numpy(), vc.cpu().numpy(),
+                                            args.cpu_budget / 3)
+        line["cpu_baseline"] = {
+            "value": round(sflops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+            "kind": "oracle", "us_per_step_sample": round(dt * 1e6, 1),
+            "host": cpu_description(), "timing": "median of 3 calls",
+            "sample": f"last {k} of {int(cu[1])} query rows of sequence 0, one "
+                      f"single-threaded oracle_prefill call"}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_prefill(args, case):
+    """The reference arm for a prefill workload: oracle_prefill on host cores."""
+    import oracle
+    orc = oracle.get()
+    n = orc.cache_bytes(0, case.num_blocks, case.block_size, case.num_kv_heads, case.head_dim)
+    kc = np.zeros(n, np.uint8)
+    vc = np.zeros(n, np.uint8)
+    orc.reshape_and_cache(case.key, case.value, kc, vc, case.slot_mapping, case.num_kv_heads,
+                          case.head_dim, case.block_size, case.num_blocks, 0)
+    per_step = min(2.0, 150.0 / max(args.steps + args.warmup, 1))
+    k, _, sflops = time_oracle_prefill(case, kc, vc, per_step)
+    ql = int(case.extra["cu_q"][1])
+    times = []
+    for i in range(args.warmup + args.steps):
+        t = time.perf_counter()
+        orc.prefill(case.q[ql - k:ql], np.array([0, k], np.int32), kc, vc,
+                    case.block_tables[:1], case.seq_lens[:1], case.num_kv_heads,
+                    case.block_size, case.num_blocks, case.scale, True, case.sliding_window)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t)
+    s = sum(times) / len(times)
+    value = sflops / s / 1e12
+    sample = (f"last {k} of {ql} query rows of sequence 0 per step, single-threaded "
+              f"oracle_prefill")
+    print(json.dumps({
+        "impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6),
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "num_seqs": case.num_seqs,
+                   "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads,
+                   "head_dim": case.head_dim, "block_size": case.block_size, "kv_dtype": "bf16"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def run_reference(args, rank, world):
     """The oracle as it stands, timed on host cores, on a bounded sample."""
     if rank != 0:
         return
     case = workload(args.workload, 0)
+    if args.workload.startswith("prefill_"):
+        run_reference_prefill(args, case)
+        return
     kv_dtype = case.kv_dtype
     import oracle
     orc = oracle.get()
@@ -658,7 +884,10 @@ def main():
     pd_build.build()
     rank, world, local = dist_init(args)
     try:
-        run_pd(args, rank, world, local)
+        if args.workload.startswith("prefill_"):
+            run_prefill(args, rank, world, local)
+        else:
+            run_pd(args, rank, world, local)
     finally:
         if world > 1:
             import torch.distributed as dist
