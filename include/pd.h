@@ -73,7 +73,9 @@ enum pd_device_flag {
   PD_DEV_BAD_SEQ_LEN = 2, /* seq_lens[b] < 0 or > max_blocks_per_seq*block_size: clamped */
   PD_DEV_BAD_SLOT = 4,    /* slot_mapping[t] >= num_blocks*block_size: token skipped */
   PD_DEV_TIMEOUT = 8,     /* a bounded wait inside a kernel gave up: that output is invalid */
-  PD_DEV_BAD_PLAN = 16    /* a balanced-plan entry was out of range: that piece skipped */
+  PD_DEV_BAD_PLAN = 16,   /* a balanced-plan entry was out of range: that piece skipped */
+  PD_DEV_BAD_SMEM = 32    /* a kernel found its shared memory off the 1024-byte boundary
+                             its swizzled tiles need: it wrote nothing */
 };
 
 /* Human-readable name of a pd_status value (static string, never NULL). */

@@ -383,6 +383,14 @@ bool use_simple_partial() {
   return simple;
 }
 
+// The tcgen05 prefill kernel runs by default; PD_PREFILL_KERNEL=mma selects
+// the mma.sync kernel instead (kept as an independent cross-check). Read on
+// every call, so that one process can run both.
+bool use_mma_sync_prefill() {
+  const char* v = getenv("PD_PREFILL_KERNEL");
+  return v != nullptr && strcmp(v, "mma") == 0;
+}
+
 }  // namespace
 }  // namespace pd
 
@@ -860,12 +868,16 @@ int pd_prefill(const void* q, int64_t q_stride, const int32_t* cu_q, const void*
   a.group = G;
   a.block_size = block_size;
   a.max_blocks_per_seq = max_blocks_per_seq;
-  a.tokens_per_cta = 64 / G;
   a.causal = causal != 0;
   a.sliding_window = sliding_window;
   a.scale_log2 = scale * kLog2e;
-  return cuda_status(launch_prefill(a, k_cache, v_cache, head_dim, max_q_len,
-                                    static_cast<cudaStream_t>(stream)));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (use_mma_sync_prefill()) {
+    a.tokens_per_cta = 64 / G;
+    return cuda_status(launch_prefill(a, k_cache, v_cache, head_dim, max_q_len, st));
+  }
+  a.tokens_per_cta = 128 / G;
+  return cuda_status(launch_prefill_umma(a, k_cache, v_cache, head_dim, max_q_len, st));
 }
 
 int pd_device_status(int32_t* flags, int32_t reset) {

@@ -233,6 +233,10 @@ cudaError_t launch_decode_partial_balanced(const DecodeArgs& a, int head_dim, in
 int balanced_ctas_per_sm(int kv_dtype, int head_dim, int group);
 cudaError_t launch_decode_combine(const CombineArgs& a, int head_dim, cudaStream_t st);
 // Paged prefill over a BF16 cache (head_dim 64 / 128); grid.x = q tiles.
+// launch_prefill: mma.sync kernel, 64 rows per CTA (tokens_per_cta = 64 / G);
+// launch_prefill_umma: tcgen05 kernel, 128 rows per CTA (128 / G).
 cudaError_t launch_prefill(const PrefillArgs& a, const void* k_cache, const void* v_cache,
                            int head_dim, int max_q_len, cudaStream_t st);
+cudaError_t launch_prefill_umma(const PrefillArgs& a, const void* k_cache, const void* v_cache,
+                                int head_dim, int max_q_len, cudaStream_t st);
 }  // namespace pd

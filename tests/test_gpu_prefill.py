@@ -5,8 +5,9 @@ cache bytes; the chunked-prefill workload at full size compares sampled
 query rows, each computed by the oracle as its own decode over the keys the
 row sees (the oracle pins make that bit-identical to oracle_prefill).
 Edge cases: empty sequences, a fresh prompt (q_len == L), one query per
-sequence, group sizes that do not divide 64 rows, a q_len above max_q_len,
-pages outside the pool, strided rows and graph replay."""
+sequence, group sizes that do not divide the CTA's rows, a q_len above
+max_q_len, pages outside the pool, strided rows and graph replay. Every test
+runs on both kernels (tcgen05 and mma.sync)."""
 import zlib
 from concurrent.futures import ThreadPoolExecutor
 
@@ -18,6 +19,17 @@ from paged_kv_split_gb300 import inputs
 from tests import gpu_util as U
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=["tcgen05", "mma_sync"], autouse=True)
+def prefill_kernel(request, monkeypatch):
+    """Every test runs on both prefill kernels: the tcgen05 one (default) and
+    the mma.sync one (PD_PREFILL_KERNEL=mma, read by libpd.so on each call)."""
+    if request.param == "mma_sync":
+        monkeypatch.setenv("PD_PREFILL_KERNEL", "mma")
+    else:
+        monkeypatch.delenv("PD_PREFILL_KERNEL", raising=False)
+    return request.param
 
 CASES = [
     # (name, seq_lens, q_lens, Hq, Hkv, D, bs, window)
