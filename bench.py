@@ -750,7 +750,10 @@ def run_prefill(args, rank, world, local):
                          f"{2 * cache_bytes / 1e6:.0f} MB rotated per step "
                          f"(L2 {l2 / 1e6:.0f} MB)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "kernel": "prefill_mma_kernel (mma.sync bf16)",
+        "roofline": {"bound": "tensor",
+                     "kernel": ("prefill_mma_kernel (mma.sync bf16)"
+                                if os.environ.get("PD_PREFILL_KERNEL") == "mma"
+                                else "prefill_umma_kernel (tcgen05 bf16, TMEM accumulators)"),
                      "achieved": round(achieved, 1), "peak": peak_t, "peak_source": peak_src,
                      "unit": "TFLOP/s", "frac": round(achieved / peak_t, 4), "traffic": None},
         "e2e": {"value": round(total_flops / (ms_e2e * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
