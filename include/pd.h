@@ -382,6 +382,9 @@ int pd_decode_static_ws(const void* q, const void* k_cache, const void* v_cache,
  * flags as in pd_decode. Supported: kv_dtype PD_KV_BF16, head_dim 64 or 128,
  * block_size 16 or 32, G = num_q_heads / num_kv_heads <= 16; anything else
  * returns PD_ERR_UNSUPPORTED. No workspace: each query tile writes its rows.
+ * The work runs on the tcgen05 tensor cores (accumulators in TMEM); with the
+ * environment variable PD_PREFILL_KERNEL=mma (read on every call) an mma.sync
+ * kernel computes the same result instead, for cross-checking.
  * Device pointers owned by the caller, 16-byte aligned; enqueued on `stream`,
  * never synchronises. */
 int pd_prefill(const void* q, int64_t q_stride, const int32_t* cu_q, const void* k_cache,
