@@ -92,6 +92,17 @@ def prefill_flops(case, rows=None) -> float:
     return 4.0 * case.head_dim * case.num_q_heads * total
 
 
+def prefill_config(name, case, world):
+    """The `config` of a prefill line, from the workload alone (both arms)."""
+    return {"workload": name, "num_seqs": case.num_seqs,
+            "query_rows": int(case.extra["cu_q"][-1]), "num_q_heads": case.num_q_heads,
+            "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim,
+            "block_size": case.block_size, "kv_dtype": "bf16", "causal": True,
+            "max_q_len": int(case.extra["q_lens"].max()), "keys_max": int(case.seq_lens.max()),
+            "flops_per_step": prefill_flops(case), "l2": L2_POLICY,
+            "parallelism": f"replicas x{world}"}
+
+
 def _with_dtype(case, kv_dtype):
     case.kv_dtype = kv_dtype
     case.name = f"{case.name}_{DTYPE_NAME[kv_dtype]}"
@@ -328,6 +339,212 @@ def build_device_state(case, kv_dtype, replicas, dev):
     return caches, ks, vs
 
 
+def workload_config(case, kv_dtype, world: int) -> dict:
+    """The `config` object of a decode line: the workload itself, computed from
+    its seeded shapes alone, so that both arms (the GPU path and the oracle)
+    print the same dict."""
+    ab = algorithmic_bytes(case, kv_dtype)
+    return {"workload": None, "num_seqs": case.num_seqs,
+            "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads,
+            "head_dim": case.head_dim, "block_size": case.block_size,
+            "kv_dtype": DTYPE_NAME[kv_dtype], "sliding_window": case.sliding_window,
+            "keys_per_step": ab["keys"], "algorithmic_bytes_per_step": int(ab["total"]),
+            "l2": L2_POLICY, "parallelism": f"replicas x{world}"}
+
+
+L2_POLICY = ("inputs larger than L2: the GPU arm rotates cache replicas whose K/V together "
+             "exceed 3x the L2, so no step reads K/V left in L2 by the previous one")
+NOMINAL_HBM_GBS = 8000.0  # the ~8 TB/s HBM3e figure the target is stated against
+
+
+def queue_ahead(steps: int) -> None:
+    """Hold the stream in a short device-side spin (torch's sleep kernel)
+    while the host enqueues the timed launches, so that a short timed region
+    measures back-to-back device execution, not host launch latency; it runs
+    before the start event and is not part of the timing."""
+    import torch
+    seconds = min(0.05, 0.002 + 60e-6 * steps)
+    torch.cuda._sleep(int(seconds * 2.0e9))
+
+
+def timed_region(stream, n, body, queue=True):
+    """Device time (ms) of n calls of body(i), CUDA events on `stream`."""
+    import torch
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if queue:
+        queue_ahead(n)
+    start.record(stream)
+    for i in range(n):
+        body(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+class DecodeSetup:
+    """Device state and the decode calls of one workload: cache replicas
+    (together more than 3x the L2, rotated per step), the schedule the host
+    lengths choose, and closures for a full step and its two kernels."""
+
+    def __init__(self, args, case, dev, schedule="auto", splits=0):
+        import torch
+        from paged_kv_split_gb300 import binding as pd
+        self.case, self.dev = case, dev
+        kv_dtype = self.kv_dtype = case.kv_dtype
+        self.ab = algorithmic_bytes(case, kv_dtype)
+        self.cache_bytes = pd.pd_cache_bytes(kv_dtype, case.num_blocks, case.block_size,
+                                             case.num_kv_heads, case.head_dim)
+        self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.replicas = max(2, math.ceil(3 * self.l2 / max(2 * self.cache_bytes, 1)))
+        self.caches, ks, vs = build_device_state(case, kv_dtype, self.replicas, dev)
+        self.ks, self.vs = ks, vs
+        q = self.q = torch.from_numpy(case.q.view(np.int16)).to(dev).view(torch.bfloat16)
+        bt = self.bt = torch.from_numpy(case.block_tables).to(dev)
+        lens = self.lens = torch.from_numpy(case.seq_lens).to(dev)
+        out = self.out = torch.empty_like(q)
+        B, hq, D = case.q.shape
+        mbs = case.max_blocks_per_seq
+        sms = self.sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        self.stream = torch.cuda.current_stream(dev)
+        G = hq // case.num_kv_heads
+        kw = self.kw = dict(num_kv_heads=case.num_kv_heads, block_size=case.block_size,
+                            num_blocks=case.num_blocks, scale=case.scale,
+                            sliding_window=case.sliding_window, kv_dtype=kv_dtype, k_scale=ks,
+                            v_scale=vs)
+        # the host holds the batch's lengths (as a serving scheduler does): the
+        # schedule (split-KV with the length-aware split count, or the balanced
+        # plan) is chosen and planned from them
+        if schedule == "auto":
+            schedule = "balanced" if (not splits and pd.pd_prefer_balanced(
+                case.seq_lens, num_q_heads=hq, num_kv_heads=case.num_kv_heads,
+                max_blocks_per_seq=mbs, block_size=case.block_size, head_dim=D,
+                sliding_window=case.sliding_window, kv_dtype=kv_dtype, num_sms=sms)) else "split"
+        self.schedule = schedule
+        if schedule == "balanced":
+            def make_plan(out_buf=None):
+                return pd.pd_balanced_plan(case.seq_lens, num_q_heads=hq,
+                                           num_kv_heads=case.num_kv_heads, head_dim=D,
+                                           block_size=case.block_size, max_blocks_per_seq=mbs,
+                                           sliding_window=case.sliding_window,
+                                           kv_dtype=kv_dtype, num_sms=sms, out=out_buf)
+            self.make_plan = make_plan
+            plan = self.plan = make_plan()
+            plan_d = self.plan_d = plan.to(dev)
+            ws = torch.zeros(max(plan.workspace_bytes, 16), dtype=torch.uint8, device=dev)
+            self.sched = {"schedule": "balanced (host plan)", "plan_ctas": plan.num_ctas,
+                          "plan_pieces": plan.num_pieces}
+            self.ws_traffic = 2 * plan.num_pieces * G * (D + 2) * 4
+
+            def decode(kc, vc, q_, bt_, lens_, out_, plan_dev=None):
+                pd.pd_decode_balanced(q_, kc, vc, bt_, plan_d if plan_dev is None else plan_dev,
+                                      plan, out_, workspace=ws, **kw)
+
+            def partial_only(kc, vc):
+                pd.pd_decode_balanced_partial(q, kc, vc, bt, plan_d, plan, out, workspace=ws,
+                                              **kw)
+
+            def combine_only(kc, vc):
+                pd.pd_decode_balanced_combine(q, kc, vc, bt, plan_d, plan, out, workspace=ws,
+                                              **kw)
+        else:
+            S = splits or pd.pd_plan_num_splits_for_lengths(
+                case.seq_lens, hq, case.num_kv_heads, mbs, case.block_size, case.sliding_window,
+                D, kv_dtype, sms)
+            ws = torch.empty(pd.pd_decode_workspace_bytes(B, hq, D, S), dtype=torch.uint8,
+                             device=dev)
+            self.sched = {"schedule": "split-KV", "num_splits": S,
+                          "split_planner": "given" if splits else "seq_lens"}
+            self.ws_traffic = 2 * B * hq * S * (D + 2) * 4
+
+            def decode(kc, vc, q_, bt_, lens_, out_, plan_dev=None):
+                pd.pd_decode(q_, kc, vc, bt_, lens_, out_, workspace=ws, num_splits=S, **kw)
+
+            def partial_only(kc, vc):
+                pd.pd_decode_partial(q, kc, vc, bt, lens, ws, num_splits=S, **kw)
+
+            def combine_only(kc, vc):
+                pd.pd_decode_combine(ws, lens, out, block_size=case.block_size,
+                                     max_blocks_per_seq=mbs, num_splits=S,
+                                     sliding_window=case.sliding_window)
+        self.decode, self.partial_only, self.combine_only = decode, partial_only, combine_only
+
+    def step(self, i):
+        # one decode step = the partial kernel, then the combine launched as its
+        # programmatic dependent, on the next cache replica
+        kc, vc = self.caches[i % self.replicas]
+        self.decode(kc, vc, self.q, self.bt, self.lens, self.out)
+
+    def partial_ms(self, n):
+        """Mean device time of the partial kernel alone (events around each
+        launch, the combine launched after each, queued ahead)."""
+        import torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        queue_ahead(2 * n)
+        for i in range(n):
+            kc, vc = self.caches[i % self.replicas]
+            evs[i][0].record(self.stream)
+            self.partial_only(kc, vc)
+            evs[i][1].record(self.stream)
+            self.combine_only(kc, vc)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    def roofline(self, part_ms, peak, peak_kind, workload_name=None):
+        partial_bytes = self.ab["kv"] + self.ab["q"] + self.ab["table"]
+        achieved = partial_bytes / (part_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "kernel": "partial (" + self.sched["schedule"] + ")",
+                "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_kind,
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+                "traffic": recorded_traffic(workload_name) if workload_name else None,
+                "algorithmic_bytes_per_launch": int(partial_bytes),
+                "partial_us_per_launch": round(part_ms * 1e3, 2)}
+
+
+def measure_workload(args, name, dev, steps=200, warmup=10):
+    """A compact figure for one more workload (the `workloads` object of the
+    default line): device-timed steps with L2 kept cold, the partial kernel's
+    roofline fraction, the schedule and the clocks. No CPU baseline, no e2e."""
+    import torch
+    case = workload(name, 0)
+    st = DecodeSetup(args, case, dev)
+    for i in range(warmup):
+        st.step(i)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_uuid(dev))
+    time.sleep(0.2)
+    w0 = time.time()
+    ms = timed_region(st.stream, steps, st.step) / steps
+    w1 = time.time()
+    time.sleep(0.1)
+    sampler.stop()
+    peak, kind = measured_peaks()
+    part = st.partial_ms(min(steps, 100))
+    gbs = st.ab["total"] / (ms * 1e-3) / 1e9
+    r = st.roofline(part, peak, kind)
+    out = {"us_per_step": round(ms * 1e3, 2), "value": round(gbs, 1), "unit": "GB/s",
+           "frac": round(gbs / peak, 4), "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+           "partial_frac": r["frac"], "partial_us": r["partial_us_per_launch"],
+           "kv_dtype": DTYPE_NAME[case.kv_dtype], "steps": steps, **st.sched,
+           "clocks": sampler.summary(w0, w1)}
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
+def gpu_uuid(dev):
+    import torch
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        return None
+
+
+EXTRA_WORKLOADS = ["long_b4_32k", "long_b4_8k", "long_b1_32k", "wide_d512", "window_d256",
+                   "quant_fp8", "quant_nvfp4"]
+
+
 def run_pd(args, rank, world, local):
     import torch
     from paged_kv_split_gb300 import binding as pd
@@ -335,134 +552,40 @@ def run_pd(args, rank, world, local):
     dev = torch.device("cuda", local if world > 1 else 0)
     case = workload(args.workload, rank)
     kv_dtype = case.kv_dtype
-    ab = algorithmic_bytes(case, kv_dtype)
-    cache_bytes = pd.pd_cache_bytes(kv_dtype, case.num_blocks, case.block_size,
-                                    case.num_kv_heads, case.head_dim)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    replicas = max(2, math.ceil(3 * l2 / max(2 * cache_bytes, 1)))
-    caches, ks, vs = build_device_state(case, kv_dtype, replicas, dev)
-    q = torch.from_numpy(case.q.view(np.int16)).to(dev).view(torch.bfloat16)
-    bt = torch.from_numpy(case.block_tables).to(dev)
-    lens = torch.from_numpy(case.seq_lens).to(dev)
-    out = torch.empty_like(q)
+    st = DecodeSetup(args, case, dev, args.schedule, args.splits)
+    ab = st.ab
     B, hq, D = case.q.shape
-    mbs = case.max_blocks_per_seq
-    # the host holds the batch's lengths (as a serving scheduler does), so the
-    # split count comes from the length-aware planner unless one is given
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    stream = torch.cuda.current_stream(dev)
-    G = hq // case.num_kv_heads
-    kw = dict(num_kv_heads=case.num_kv_heads, block_size=case.block_size,
-              num_blocks=case.num_blocks, scale=case.scale, sliding_window=case.sliding_window,
-              kv_dtype=kv_dtype, k_scale=ks, v_scale=vs)
-    # the host holds the batch's lengths (as a serving scheduler does): the
-    # schedule (split-KV with the length-aware split count, or the balanced
-    # plan) is chosen and planned from them
-    schedule = args.schedule
-    if schedule == "auto":
-        schedule = "balanced" if (not args.splits and pd.pd_prefer_balanced(
-            case.seq_lens, num_q_heads=hq, num_kv_heads=case.num_kv_heads,
-            max_blocks_per_seq=mbs, block_size=case.block_size, head_dim=D,
-            sliding_window=case.sliding_window, kv_dtype=kv_dtype, num_sms=sms)) else "split"
-    if schedule == "balanced":
-        def make_plan(out_buf=None):
-            return pd.pd_balanced_plan(case.seq_lens, num_q_heads=hq,
-                                       num_kv_heads=case.num_kv_heads, head_dim=D,
-                                       block_size=case.block_size, max_blocks_per_seq=mbs,
-                                       sliding_window=case.sliding_window, kv_dtype=kv_dtype,
-                                       num_sms=sms, out=out_buf)
-        plan = make_plan()
-        plan_d = plan.to(dev)
-        ws = torch.zeros(max(plan.workspace_bytes, 16), dtype=torch.uint8, device=dev)
-        S = None
-        sched_cfg = {"schedule": "balanced (host plan)", "plan_ctas": plan.num_ctas,
-                     "plan_pieces": plan.num_pieces}
-        ws_traffic = 2 * plan.num_pieces * G * (D + 2) * 4
-
-        def decode(kc, vc, q_, bt_, lens_, out_, plan_dev=None):
-            pd.pd_decode_balanced(q_, kc, vc, bt_, plan_d if plan_dev is None else plan_dev,
-                                  plan, out_, workspace=ws, **kw)
-
-        def partial_only(kc, vc):
-            pd.pd_decode_balanced_partial(q, kc, vc, bt, plan_d, plan, out, workspace=ws, **kw)
-
-        def combine_only(kc, vc):
-            pd.pd_decode_balanced_combine(q, kc, vc, bt, plan_d, plan, out, workspace=ws, **kw)
-    else:
-        S = args.splits or pd.pd_plan_num_splits_for_lengths(
-            case.seq_lens, hq, case.num_kv_heads, mbs, case.block_size, case.sliding_window, D,
-            kv_dtype, sms)
-        ws = torch.empty(pd.pd_decode_workspace_bytes(B, hq, D, S), dtype=torch.uint8,
-                         device=dev)
-        sched_cfg = {"schedule": "split-KV", "num_splits": S,
-                     "split_planner": "given" if args.splits else "seq_lens"}
-        ws_traffic = 2 * B * hq * S * (D + 2) * 4
-
-        def decode(kc, vc, q_, bt_, lens_, out_, plan_dev=None):
-            pd.pd_decode(q_, kc, vc, bt_, lens_, out_, workspace=ws, num_splits=S, **kw)
-
-        def partial_only(kc, vc):
-            pd.pd_decode_partial(q, kc, vc, bt, lens, ws, num_splits=S, **kw)
-
-        def combine_only(kc, vc):
-            pd.pd_decode_combine(ws, lens, out, block_size=case.block_size,
-                                 max_blocks_per_seq=mbs, num_splits=S,
-                                 sliding_window=case.sliding_window)
-
-    def step(i):
-        # one decode step = the partial kernel, then the combine launched as
-        # its programmatic dependent
-        kc, vc = caches[i % replicas]
-        decode(kc, vc, q, bt, lens, out)
-
-    def split_step(i, ev):
-        # the same two kernels launched separately, with events around the
-        # partial kernel (the roofline's kernel)
-        kc, vc = caches[i % replicas]
-        ev[0].record(stream)
-        partial_only(kc, vc)
-        ev[1].record(stream)
-        combine_only(kc, vc)
+    stream = st.stream
+    replicas, caches = st.replicas, st.caches
+    q, bt, lens, out = st.q, st.bt, st.lens, st.out
+    decode, step = st.decode, st.step
 
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
 
-    uuid = None
-    try:
-        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        uuid = None
-    sampler = ClockSampler(uuid)
+    sampler = ClockSampler(gpu_uuid(dev))
     time.sleep(0.3)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
     w0 = time.time()
-    start.record(stream)
-    for i in range(args.steps):
-        step(i)
-    end.record(stream)
-    torch.cuda.synchronize(dev)
+    total_ms = timed_region(stream, args.steps, step)
     w1 = time.time()
     barrier(world)
-    total_ms = start.elapsed_time(end)
     time.sleep(0.1)
     sampler.stop()
     clocks = sampler.summary(w0, w1)
-    # the partial kernel's own duration, over the same number of steps
+    # the partial kernel's own duration (events around each launch)
     n_inst = min(args.steps, 500)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n_inst)]
-    for i in range(n_inst):
-        split_step(i, evs[i])
-    torch.cuda.synchronize(dev)
-    partial_ms = [a.elapsed_time(b) for a, b in evs]
+    part_ms = st.partial_ms(n_inst)
 
-    # per-step spread of the whole decode step (events around each pd_decode)
+    # per-step spread of the whole decode step (events around each pd_decode:
+    # the event between steps also ends the programmatic overlap of the next
+    # step's partial grid with this step's combine)
     n_dist = min(args.steps, 500)
     evd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(n_dist)]
+    queue_ahead(n_dist)
     for i in range(n_dist):
         evd[i][0].record(stream)
         step(i)
@@ -475,28 +598,21 @@ def run_pd(args, rank, world, local):
     # in L2 as far as it fits (the headline rotates replicas past L2)
     n_hot = min(args.steps, 1000)
     for _ in range(3):
-        step(0)
+        kc, vc = caches[0]
+        decode(kc, vc, q, bt, lens, out)
     torch.cuda.synchronize(dev)
-    eh0, eh1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    eh0.record(stream)
-    for _ in range(n_hot):
-        step(0)
-    eh1.record(stream)
-    torch.cuda.synchronize(dev)
-    hot_us = eh0.elapsed_time(eh1) * 1e3 / n_hot
+
+    def hot_step(i):
+        kc, vc = caches[0]
+        decode(kc, vc, q, bt, lens, out)
+    hot_us = timed_region(stream, n_hot, hot_step) * 1e3 / n_hot
 
     # the same step captured in CUDA graphs (one per cache replica), replayed in rotation
     def timed_replays(graphs, n):
         for i in range(3):
             graphs[i % len(graphs)].replay()
         torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(n):
-            graphs[i % len(graphs)].replay()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1) * 1e3 / n
+        return timed_region(stream, n, lambda i: graphs[i % len(graphs)].replay()) * 1e3 / n
 
     n_graph = min(args.steps, 2000)
     graphs = []
@@ -524,27 +640,20 @@ def run_pd(args, rank, world, local):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             pd.pd_reshape_and_cache(new_k, new_v, kc, vc, slots_new, num_blocks=case.num_blocks,
-                                    block_size=case.block_size, kv_dtype=kv_dtype, k_scale=ks,
-                                    v_scale=vs)
+                                    block_size=case.block_size, kv_dtype=kv_dtype,
+                                    k_scale=st.ks, v_scale=st.vs)
             decode(kc, vc, q, bt, lens, out)
         graphs_w.append(g)
     graph_w_us = timed_replays(graphs_w, n_graph)
+    del graphs, graphs_w
 
     ms_step_local = total_ms / args.steps
     ms_step, total_bytes, value = job_throughput(ms_step_local, ab["total"], world)
 
     # roofline of the dominant kernel (the split-KV partial)
-    part_ms = statistics.mean(partial_ms)
-    partial_bytes = ab["kv"] + ab["q"] + ab["table"]
     peak, peak_kind = measured_peaks()
-    achieved = partial_bytes / (part_ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "partial (" + sched_cfg["schedule"] + ")",
-                "achieved": round(achieved, 1),
-                "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(args.workload),
-                "algorithmic_bytes_per_launch": int(partial_bytes),
-                "partial_us_per_launch": round(part_ms * 1e3, 2),
-                "timed_launches": n_inst}
+    roofline = st.roofline(part_ms, peak, peak_kind, args.workload)
+    roofline["timed_launches"] = n_inst
 
     # e2e: through the C ABI from pinned host buffers, copies inside the timing
     q_h = torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -554,19 +663,19 @@ def run_pd(args, rank, world, local):
     q_d, bt_d, lens_d = torch.empty_like(q), torch.empty_like(bt), torch.empty_like(lens)
     e2e_steps = max(10, min(args.steps, 200))
     plan_bytes = 0
-    if schedule == "balanced":
-        plan_h = pd.balanced_plan_buffer(B, case.num_kv_heads, sms, pin=True)
-        plan_dd = torch.empty_like(plan_d)
-        plan_bytes = plan_d.numel() * 4
+    if st.schedule == "balanced":
+        plan_h = pd.balanced_plan_buffer(B, case.num_kv_heads, st.sms, pin=True)
+        plan_dd = torch.empty_like(st.plan_d)
+        plan_bytes = st.plan_d.numel() * 4
 
     def e2e_step(i):
         kc, vc = caches[i % replicas]
         q_d.copy_(q_h, non_blocking=True)
         bt_d.copy_(bt_h, non_blocking=True)
         lens_d.copy_(lens_h, non_blocking=True)
-        if schedule == "balanced":
+        if st.schedule == "balanced":
             # the scheduler plans every step (lengths change as tokens arrive)
-            make_plan(plan_h)  # plans straight into the pinned buffer
+            st.make_plan(plan_h)  # plans straight into the pinned buffer
             plan_dd.copy_(plan_h, non_blocking=True)
             decode(kc, vc, q_d, bt_d, lens_d, out, plan_dev=plan_dd)
         else:
@@ -590,38 +699,44 @@ def run_pd(args, rank, world, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         kc, vc = caches[0]
-        k, dt, sab = time_oracle(case, kv_dtype, kc.cpu().numpy(), vc.cpu().numpy(), ks, vs,
-                                 args.cpu_budget)
+        k, dt, sab = time_oracle(case, kv_dtype, kc.cpu().numpy(), vc.cpu().numpy(), st.ks,
+                                 st.vs, args.cpu_budget)
         cpu = {"value": round(sab["total"] / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
                "kind": "oracle", "us_per_step_sample": round(dt * 1e6, 1),
                "host": cpu_description(), "timing": "median of 3 calls",
                "sample": f"first {k} of {case.num_seqs} sequences of the same batch "
                          f"({sab['keys']} keys), one single-threaded oracle_decode call"}
+    sched, ws_traffic = st.sched, st.ws_traffic
+    del st, caches
+    torch.cuda.empty_cache()
+
+    # the other configurations, compact (rank 0 of a one-GPU run; skipped with
+    # --workloads none)
+    extra = None
+    if rank == 0 and world == 1 and args.workloads != "none":
+        names = EXTRA_WORKLOADS if args.workloads == "all" else args.workloads.split(",")
+        extra = {n: measure_workload(args, n, dev) for n in names if n != args.workload}
 
     if rank == 0:
+        config = workload_config(case, kv_dtype, world)
+        config["workload"] = args.workload
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
             "us_per_step": round(ms_step * 1e3, 2),
             "pct_of_hbm_peak": round(100 * value / peak, 2),
+            "pct_of_nominal_8tbs": round(100 * value / NOMINAL_HBM_GBS, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": DTYPE_NAME[kv_dtype], "data": "synthetic",
-            "config": {"workload": args.workload, "num_seqs": B, "num_q_heads": hq,
-                       "num_kv_heads": case.num_kv_heads, "head_dim": D,
-                       "block_size": case.block_size, "kv_dtype": DTYPE_NAME[kv_dtype],
-                       "sliding_window": case.sliding_window, **sched_cfg,
-                       "keys_per_step": ab["keys"], "algorithmic_bytes_per_step": int(ab["total"]),
-                       "workspace_bytes_per_step": int(ws_traffic),
-                       "l2": f"inputs larger than L2: {replicas} cache replicas of "
-                             f"{2 * cache_bytes / 1e6:.0f} MB rotated per step "
-                             f"(L2 {l2 / 1e6:.0f} MB)",
-                       "parallelism": f"replicas x{world}"},
+            "config": config,
+            "schedule": {**sched, "workspace_bytes_per_step": int(ws_traffic),
+                         "cache_replicas": replicas},
             "step_us": spread,
             "hot_l2": {"us_per_step": round(hot_us, 2),
                        "value": round(ab["total"] / (hot_us * 1e-6) / 1e9, 1), "unit": "GB/s",
                        "note": "one cache replica reused every step (K/V "
-                               f"{2 * cache_bytes / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB): "
-                               "L2-warm, not the headline"},
+                               f"{2 * st_cache_mb(case, kv_dtype):.0f} MB): L2-warm, "
+                               "not the headline"},
             "graph": {"us_per_step": round(graph_us, 2),
                       "value": round(ab["total"] / (graph_us * 1e-6) / 1e9, 1), "unit": "GB/s",
                       "note": "pd_decode captured in one CUDA graph per cache replica"},
@@ -631,8 +746,15 @@ def run_pd(args, rank, world, local):
                                          "pd_decode, captured in one CUDA graph"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": 2 * args.steps, "clocks": clocks,
+            "workloads": extra,
         }
         print(json.dumps(line), flush=True)
+
+
+def st_cache_mb(case, kv_dtype):
+    from paged_kv_split_gb300 import binding as pd
+    return pd.pd_cache_bytes(kv_dtype, case.num_blocks, case.block_size, case.num_kv_heads,
+                             case.head_dim) / 1e6
 
 
 def time_oracle_prefill(case, kc_host, vc_host, budget_s: float):
@@ -682,7 +804,8 @@ def run_prefill(args, rank, world, local):
     lens = torch.from_numpy(case.seq_lens).to(dev)
     kw = dict(max_q_len=max_q, num_kv_heads=case.num_kv_heads, block_size=case.block_size,
               num_blocks=case.num_blocks, scale=case.scale, causal=True,
-              sliding_window=case.sliding_window)
+              sliding_window=case.sliding_window,
+              crosscheck=args.prefill_kernel == "mma_sync")
 
     def step(i):
         kc, vc = caches[i % replicas]
@@ -702,14 +825,9 @@ def run_prefill(args, rank, world, local):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t0 = time.time()
-    e0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    ms_local = timed_region(stream, args.steps, step) / args.steps
     t1 = time.time()
     barrier(world)
-    ms_local = e0.elapsed_time(e1) / args.steps
     ms_step = max_over_ranks(ms_local, world)
     total_flops = sum_over_ranks(flops, world)
     tflops = total_flops / (ms_step * 1e-3) / 1e12
@@ -760,18 +878,11 @@ def run_prefill(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "us_per_step": round(ms_step * 1e3, 1), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "num_seqs": case.num_seqs, "query_rows": T,
-                   "num_q_heads": hq, "num_kv_heads": case.num_kv_heads, "head_dim": D,
-                   "block_size": case.block_size, "kv_dtype": "bf16", "causal": True,
-                   "max_q_len": max_q, "keys_max": int(case.seq_lens.max()),
-                   "flops_per_step": flops,
-                   "l2": f"inputs larger than L2: {replicas} cache replicas of "
-                         f"{2 * cache_bytes / 1e6:.0f} MB rotated per step "
-                         f"(L2 {l2 / 1e6:.0f} MB)",
-                   "parallelism": f"replicas x{world}"},
+        "config": prefill_config(args.workload, case, world),
+        "cache_replicas": replicas,
         "roofline": {"bound": "tensor",
-                     "kernel": ("prefill_mma_kernel (mma.sync bf16)"
-                                if os.environ.get("PD_PREFILL_KERNEL") == "mma"
+                     "kernel": ("prefill_mma_kernel (mma.sync bf16, pd_prefill_crosscheck)"
+                                if args.prefill_kernel == "mma_sync"
                                 else "prefill_umma_kernel (tcgen05 bf16, TMEM accumulators)"),
                      "achieved": round(achieved, 1), "peak": peak_t, "peak_source": peak_src,
                      "unit": "TFLOP/s", "frac": round(achieved / peak_t, 4), "traffic": None},
@@ -823,9 +934,7 @@ def run_reference_prefill(args, case):
         "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "num_seqs": case.num_seqs,
-                   "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads,
-                   "head_dim": case.head_dim, "block_size": case.block_size, "kv_dtype": "bf16"},
+        "config": prefill_config(args.workload, case, 1),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": 1,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -873,10 +982,7 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": DTYPE_NAME[kv_dtype], "data": "synthetic",
-        "config": {"workload": args.workload, "num_seqs": case.num_seqs,
-                   "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads,
-                   "head_dim": case.head_dim, "block_size": case.block_size,
-                   "kv_dtype": DTYPE_NAME[kv_dtype]},
+        "config": {**workload_config(case, kv_dtype, world), "workload": args.workload},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -895,6 +1001,10 @@ def main():
     ap.add_argument("--schedule", default="auto", choices=["auto", "split", "balanced"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workloads", default="all",
+                    help="the other decode configurations measured compactly into the line's "
+                         "`workloads` object: all, none, or a comma-separated list")
+    ap.add_argument("--prefill-kernel", default="tcgen05", choices=["tcgen05", "mma_sync"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))

@@ -117,8 +117,23 @@ int pd_reshape_and_cache(const void* key, const void* value, void* k_cache, void
 /* Max |x| over n bf16 values, folded into *out_max with an atomic max
  * ([metrale] `bf16_absmax`: "The caller zeroes out_max first"). NaN values
  * are skipped. data: device bf16 [n]; out_max: device float, caller-zeroed.
- * Used for FP8 calibration: k_scale = absmax(K) / 448 (1 if absmax is 0). */
+ * The first half of FP8 calibration; pd_fp8_scale / pd_fp8_scales_from_absmax
+ * turn the maximum into the per-tensor scale. */
 int pd_absmax_bf16(const void* data, int64_t n, float* out_max, void* stream);
+
+/* FP8 calibration scale of one tensor from its absmax ([metrale] `bf16_absmax`:
+ * the FP8 KV calibration runs it before each K / V pair; the scale maps the
+ * tensor's largest magnitude onto E4M3's largest finite value, 448):
+ * absmax / 448 in IEEE fp32 division, or 1.0 when absmax is not > 0 (an
+ * all-zero tensor; NaN). Host only, no CUDA call. Pass the result as
+ * pd_reshape_and_cache's k_scale / v_scale and pd_decode's. */
+float pd_fp8_scale(float absmax);
+
+/* The same on the device: scales[i] = pd_fp8_scale(absmax[i]) for i < count,
+ * with absmax the outputs of pd_absmax_bf16 (device float [count]) and scales
+ * device float [count] (4-byte aligned). Enqueued on `stream`, no
+ * synchronisation: a caller reads the scales back once, after calibration. */
+int pd_fp8_scales_from_absmax(const float* absmax, float* scales, int32_t count, void* stream);
 
 /* Workspace bytes that pd_decode / pd_decode_partial need for num_splits
  * partials: per (sequence, q head, split) head_dim fp32 values of the
@@ -202,6 +217,27 @@ int pd_decode_strided(const void* q, int64_t q_stride, const void* k_cache, cons
                       int32_t num_splits, int32_t sliding_window, int32_t kv_dtype,
                       float k_scale, float v_scale, void* workspace, size_t workspace_bytes,
                       void* stream);
+
+/* pd_decode writing the output as E4M3 bytes instead of bf16 (the "E4M3
+ * output variant" that [AstrAI] lists beside stride-based addressing; the
+ * pages define no output scale or rounding, so this library's reading is):
+ *   out[b, h, d] = E4M3(o[b, h, d] / out_scale)
+ * with o the fp32 attention output (before any bf16 rounding), out_scale a
+ * per-tensor fp32 scale (finite, > 0; PD_ERR_INVALID_ARG otherwise), IEEE
+ * fp32 division and pd_reshape_and_cache's E4M3 rules (nearest, ties to
+ * even, saturation to +-448, the sign of a zero kept). A code c stands for
+ * decode(c) * out_scale. out: device uint8 [num_seqs][num_q_heads][head_dim],
+ * 16-byte aligned. Every sequence's partials go through the workspace (no
+ * direct single-split write), so workspace_bytes >=
+ * pd_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, S). Everything
+ * else as pd_decode. */
+int pd_decode_e4m3_out(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* seq_lens, void* out,
+                       int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
+                       int64_t num_blocks, float scale, int32_t num_splits,
+                       int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
+                       float out_scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /* The first half of pd_decode alone: writes the S partials (O_s normalised,
  * m_s, l_s) of every (sequence, q head) to the workspace ([metrale]: "each
@@ -382,9 +418,7 @@ int pd_decode_static_ws(const void* q, const void* k_cache, const void* v_cache,
  * flags as in pd_decode. Supported: kv_dtype PD_KV_BF16, head_dim 64 or 128,
  * block_size 16 or 32, G = num_q_heads / num_kv_heads <= 16; anything else
  * returns PD_ERR_UNSUPPORTED. No workspace: each query tile writes its rows.
- * The work runs on the tcgen05 tensor cores (accumulators in TMEM); with the
- * environment variable PD_PREFILL_KERNEL=mma (read on every call) an mma.sync
- * kernel computes the same result instead, for cross-checking.
+ * The work runs on the tcgen05 tensor cores (accumulators in TMEM).
  * Device pointers owned by the caller, 16-byte aligned; enqueued on `stream`,
  * never synchronises. */
 int pd_prefill(const void* q, int64_t q_stride, const int32_t* cu_q, const void* k_cache,
@@ -394,6 +428,56 @@ int pd_prefill(const void* q, int64_t q_stride, const int32_t* cu_q, const void*
                int32_t max_blocks_per_seq, int64_t num_blocks, float scale, int32_t causal,
                int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
                void* stream);
+
+/* ---- Cross-check kernels ----
+ * Independent second implementations of two steps, kept to test the fast
+ * kernels against: same arguments, same results up to fp32 summation order.
+ * They are slower and never chosen by the calls above. */
+
+/* pd_decode with the split-KV partials computed on CUDA cores (one warp per
+ * key for the scores, plain fp32 loops for P V) instead of the tensor-core
+ * kernel; every partial goes through the workspace and the combine. */
+int pd_decode_crosscheck(const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, const int32_t* seq_lens, void* out,
+                         int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
+                         int64_t num_blocks, float scale, int32_t num_splits,
+                         int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* pd_prefill on mma.sync tensor-core tiles (64 query rows per CTA) instead of
+ * the tcgen05 kernel. Same arguments and support as pd_prefill. */
+int pd_prefill_crosscheck(const void* q, int64_t q_stride, const int32_t* cu_q,
+                          const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                          const int32_t* seq_lens, void* out, int64_t out_stride,
+                          int32_t num_seqs, int32_t max_q_len, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                          int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
+                          int32_t causal, int32_t sliding_window, int32_t kv_dtype,
+                          float k_scale, float v_scale, void* stream);
+
+/* ---- Test hooks ----
+ * For the library's own tests; a serving process has no reason to call them. */
+
+/* Run the cache write's own device encoders on fp32 bit patterns:
+ * codes[i] = code of the float whose bits are first_bits + i (mod 2^32), for
+ * i < count <= 2^32; format 0 = E4M3 (the FP8 cache, rules of
+ * pd_reshape_and_cache), 1 = E2M1 (the NVFP4 values). codes: device uint8
+ * [count]. Lets a test compare the encoders with a reference over every fp32
+ * input, including quotients no bf16 input and scale produce. */
+int pd_test_encode(int32_t format, uint32_t first_bits, int64_t count, uint8_t* codes,
+                   void* stream);
+
+/* Set the limit (ns) of the decode partial kernels' consumer-side waits for a
+ * stage of keys, for calls made after it; 0xFFFFFFFF restores the default
+ * (2 s). Returns the previous limit. A test sets it to 0 so that those waits
+ * run out at once, to see the bounded-wait path report PD_DEV_TIMEOUT and the
+ * kernel end normally: a consumer warp that gives up stops handing stages
+ * back and raises its CTA's abort word; the producer then issues nothing more
+ * and waits for every copy it already issued before the CTA ends. The outputs
+ * of such a call are invalid. Process-wide, not thread-safe against
+ * concurrent decode calls. */
+uint32_t pd_test_set_consumer_wait_ns(uint32_t ns);
 
 /* Read (and, if reset != 0, clear) the pd_device_flag bits that kernels on
  * the current device have raised since the last reset. Synchronises the

@@ -74,6 +74,9 @@ class Oracle:
         L.oracle_decode.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64,
                                     f32, i32, i32, f32, f32]
         L.oracle_decode.restype = ctypes.c_int
+        L.oracle_decode_e4m3_out.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                             i64, f32, i32, i32, f32, f32, f32]
+        L.oracle_decode_e4m3_out.restype = ctypes.c_int
         L.oracle_prefill.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64,
                                      f32, i32, i32, i32, f32, f32]
         L.oracle_prefill.restype = ctypes.c_int
@@ -160,6 +163,24 @@ class Oracle:
             raise ValueError("oracle_decode: invalid arguments")
         return out, out_f32
 
+
+    def decode_e4m3_out(self, q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads,
+                        block_size, num_blocks, scale, out_scale, sliding_window=0,
+                        kv_dtype=KV_BF16, k_scale=1.0, v_scale=1.0):
+        """Decode with E4M3 output: codes uint8 [B, Hq, D] = E4M3(o / out_scale)."""
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        block_tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+        seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        B, Hq, D = q.shape
+        codes = np.empty((B, Hq, D), np.uint8)
+        rc = self.lib.oracle_decode_e4m3_out(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens),
+            _ptr(codes), B, Hq, num_kv_heads, D, block_size, block_tables.shape[1], num_blocks,
+            float(scale), int(sliding_window), kv_dtype, float(k_scale), float(v_scale),
+            float(out_scale))
+        if rc != 0:
+            raise ValueError("oracle_decode_e4m3_out: invalid arguments")
+        return codes
 
     def prefill(self, q, cu_q, k_cache, v_cache, block_tables, seq_lens, num_kv_heads,
                 block_size, num_blocks, scale, causal=True, sliding_window=0, kv_dtype=KV_BF16,

@@ -393,6 +393,35 @@ int oracle_decode(const uint16_t* q, const uint8_t* k_cache, const uint8_t* v_ca
   return 0;
 }
 
+/* Decode with E4M3 output codes (the "E4M3 output variant" the AstrAI
+ * "csrc/tests" log names beside stride-based addressing, which the pages do
+ * not define further). Reading taken: out_codes[b, h, d] =
+ * E4M3(o[b, h, d] / out_scale), where o is the fp32 attention output that
+ * oracle_decode computes before its bf16 rounding, out_scale a per-tensor
+ * fp32 scale (finite, > 0), the division IEEE fp32, and the encoder the
+ * cache's (nearest, ties to even, saturation to +-448, sign of zero kept).
+ * The stored code decodes to code * out_scale. Returns 0, or -1 as
+ * oracle_decode (or for a bad out_scale). */
+int oracle_decode_e4m3_out(const uint16_t* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                           const int32_t* block_tables, const int32_t* seq_lens,
+                           uint8_t* out_codes, int32_t num_seqs, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                           int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
+                           int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
+                           float out_scale) {
+  if (!(std::isfinite(out_scale) && out_scale > 0.0f)) return -1;
+  const size_t n = static_cast<size_t>(num_seqs) * num_q_heads * head_dim;
+  std::vector<uint16_t> out_bf16(n);
+  std::vector<float> o(n);
+  const int rc = oracle_decode(q, k_cache, v_cache, block_tables, seq_lens, out_bf16.data(),
+                               o.data(), num_seqs, num_q_heads, num_kv_heads, head_dim,
+                               block_size, max_blocks_per_seq, num_blocks, scale,
+                               sliding_window, kv_dtype, k_scale, v_scale);
+  if (rc != 0) return rc;
+  for (size_t i = 0; i < n; ++i) out_codes[i] = e4m3_code(quotient(o[i], out_scale));
+  return 0;
+}
+
 /* Paged prefill (chunked prefill) attention over the same caches: several
  * query tokens per sequence. The pages name this unit beside decode
  * (pegainfer issue 1008: `prefill_paged_launch` over the paged-KV view;

@@ -45,9 +45,20 @@ _lib.pd_reshape_and_cache.argtypes = [_P, _P, _P, _P, _P, _i32, _i32, _i32, _i32
                                       _f32, _f32, _P]
 _lib.pd_reshape_and_cache.restype = ctypes.c_int
 _lib.pd_absmax_bf16.argtypes, _lib.pd_absmax_bf16.restype = [_P, _i64, _P, _P], ctypes.c_int
+_lib.pd_fp8_scale.argtypes, _lib.pd_fp8_scale.restype = [_f32], _f32
+_lib.pd_fp8_scales_from_absmax.argtypes = [_P, _P, _i32, _P]
+_lib.pd_fp8_scales_from_absmax.restype = ctypes.c_int
+_lib.pd_test_encode.argtypes, _lib.pd_test_encode.restype = [_i32, ctypes.c_uint32, _i64, _P,
+                                                              _P], ctypes.c_int
+_lib.pd_test_set_consumer_wait_ns.argtypes = [ctypes.c_uint32]
+_lib.pd_test_set_consumer_wait_ns.restype = ctypes.c_uint32
 _DECODE_ARGS = [_P, _P, _P, _P, _P, _P, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _f32, _i32,
                 _i32, _i32, _f32, _f32, _P, _sz, _P]
 _lib.pd_decode.argtypes, _lib.pd_decode.restype = _DECODE_ARGS, ctypes.c_int
+_lib.pd_decode_crosscheck.argtypes = _DECODE_ARGS
+_lib.pd_decode_crosscheck.restype = ctypes.c_int
+_lib.pd_decode_e4m3_out.argtypes = _DECODE_ARGS[:19] + [_f32] + _DECODE_ARGS[19:]
+_lib.pd_decode_e4m3_out.restype = ctypes.c_int
 _lib.pd_decode_strided.argtypes = [_P, _i64] + _DECODE_ARGS[1:6] + [_i64] + _DECODE_ARGS[6:]
 _lib.pd_decode_strided.restype = ctypes.c_int
 _lib.pd_decode_partial.argtypes = [_P, _P, _P, _P, _P, _i32, _i32, _i32, _i32, _i32, _i32, _i64,
@@ -59,6 +70,8 @@ _lib.pd_device_status.argtypes, _lib.pd_device_status.restype = [_P, _i32], ctyp
 _lib.pd_prefill.argtypes = [_P, _i64, _P, _P, _P, _P, _P, _P, _i64, _i32, _i32, _i32, _i32, _i32,
                             _i32, _i32, _i64, _f32, _i32, _i32, _i32, _f32, _f32, _P]
 _lib.pd_prefill.restype = ctypes.c_int
+_lib.pd_prefill_crosscheck.argtypes = _lib.pd_prefill.argtypes
+_lib.pd_prefill_crosscheck.restype = ctypes.c_int
 _lib.pd_prefer_balanced.argtypes = [_P, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]
 _lib.pd_prefer_balanced.restype = ctypes.c_int
 _lib.pd_balanced_plan_bytes.argtypes = [_i32, _i32, _i32]
@@ -200,18 +213,47 @@ def pd_absmax_bf16(data, out_max, stream=None) -> None:
     _check("pd_absmax_bf16", rc)
 
 
-def fp8_calibrate(key, value, stream=None):
-    """Per-tensor FP8 scales (absmax / 448, 1.0 when absmax is 0) for key and value.
+def pd_fp8_scale(absmax: float) -> float:
+    """FP8 scale of a tensor from its absmax (libpd.so's pd_fp8_scale)."""
+    return float(_lib.pd_fp8_scale(float(absmax)))
 
-    Runs pd_absmax_bf16 on the device, then reads the two maxima back (one
-    synchronising copy: calibration is a one-off step, not part of decode)."""
+
+def pd_fp8_scales_from_absmax(absmax, scales, stream=None) -> None:
+    """scales[i] = pd_fp8_scale(absmax[i]) on the device (float32 tensors)."""
+    if absmax.shape != scales.shape:
+        raise ValueError("absmax and scales must have the same shape")
+    rc = _lib.pd_fp8_scales_from_absmax(_dev(absmax, "absmax", torch.float32),
+                                        _dev(scales, "scales", torch.float32, absmax.device),
+                                        absmax.numel(), _stream(stream))
+    _check("pd_fp8_scales_from_absmax", rc)
+
+
+def fp8_calibrate(key, value, stream=None):
+    """Per-tensor FP8 scales for key and value: pd_absmax_bf16 of each, then
+    pd_fp8_scales_from_absmax, both on the device; the two scales are read
+    back once (a synchronising copy: calibration is a one-off step, not part
+    of decode)."""
     amax = torch.zeros(2, dtype=torch.float32, device=key.device)
     pd_absmax_bf16(key, amax[0:1], stream)
     pd_absmax_bf16(value, amax[1:2], stream)
-    a = amax.cpu()
-    scales = torch.where(a > 0, a / torch.tensor(448.0, dtype=torch.float32),
-                         torch.ones_like(a))
-    return float(scales[0]), float(scales[1])
+    scales = torch.empty_like(amax)
+    pd_fp8_scales_from_absmax(amax, scales, stream)
+    ks, vs = scales.cpu().tolist()
+    return ks, vs
+
+
+def pd_test_encode(fmt: int, first_bits: int, codes, stream=None) -> None:
+    """Test hook: codes[i] = the device encoder's code (0 = E4M3, 1 = E2M1) of
+    the fp32 bit pattern first_bits + i (codes: CUDA uint8 tensor)."""
+    rc = _lib.pd_test_encode(int(fmt), int(first_bits) & 0xFFFFFFFF, codes.numel(),
+                             _dev(codes, "codes", torch.uint8), _stream(stream))
+    _check("pd_test_encode", rc)
+
+
+def pd_test_set_consumer_wait_ns(ns: int) -> int:
+    """Test hook: the decode kernels' consumer wait limit (0xFFFFFFFF = default).
+    Returns the previous limit."""
+    return int(_lib.pd_test_set_consumer_wait_ns(int(ns) & 0xFFFFFFFF))
 
 
 def _decode_shape(q, block_tables, seq_lens, out=None):
@@ -227,11 +269,12 @@ def _decode_shape(q, block_tables, seq_lens, out=None):
 
 def pd_decode(q, k_cache, v_cache, block_tables, seq_lens, out, *, num_kv_heads, block_size,
               num_blocks, scale, num_splits=0, sliding_window=0, kv_dtype=PD_KV_BF16,
-              k_scale=1.0, v_scale=1.0, workspace=None, stream=None):
+              k_scale=1.0, v_scale=1.0, workspace=None, stream=None, crosscheck=False):
     """One decode step (split-KV partials + combine) into out (bf16 [B, Hq, D]).
 
     workspace: a CUDA uint8 tensor of at least pd_decode_workspace_bytes for
-    the split count used; when None, one is allocated here with torch."""
+    the split count used; when None, one is allocated here with torch.
+    crosscheck: call pd_decode_crosscheck (the CUDA-core partial kernel)."""
     B, hq, d, mbs = _decode_shape(q, block_tables, seq_lens, out)
     code = _dtype_code(kv_dtype)
     S = num_splits
@@ -242,14 +285,44 @@ def pd_decode(q, k_cache, v_cache, block_tables, seq_lens, out, *, num_kv_heads,
         workspace = torch.empty(max(pd_decode_workspace_bytes(B, hq, d, S), 16), dtype=torch.uint8,
                                 device=q.device)
     dev = q.device
-    rc = _lib.pd_decode(
+    fn = "pd_decode_crosscheck" if crosscheck else "pd_decode"
+    rc = getattr(_lib, fn)(
         _dev(q, "q", torch.bfloat16, dev), _dev(k_cache, "k_cache", None, dev),
         _dev(v_cache, "v_cache", None, dev), _dev(block_tables, "block_tables", torch.int32, dev),
         _dev(seq_lens, "seq_lens", torch.int32, dev), _dev(out, "out", torch.bfloat16, dev), B,
         hq, num_kv_heads, d, block_size, mbs, num_blocks, float(scale), S, sliding_window, code,
         float(k_scale), float(v_scale), _dev(workspace, "workspace", None, dev),
         workspace.numel() * workspace.element_size(), _stream(stream))
-    _check("pd_decode", rc)
+    _check(fn, rc)
+    return out
+
+
+def pd_decode_e4m3_out(q, k_cache, v_cache, block_tables, seq_lens, out, *, out_scale,
+                       num_kv_heads, block_size, num_blocks, scale, num_splits=0,
+                       sliding_window=0, kv_dtype=PD_KV_BF16, k_scale=1.0, v_scale=1.0,
+                       workspace=None, stream=None):
+    """One decode step writing E4M3 codes E4M3(o / out_scale) into out
+    (uint8 [B, Hq, D]); otherwise as pd_decode."""
+    B, hq, d, mbs = _decode_shape(q, block_tables, seq_lens)
+    if tuple(out.shape) != (B, hq, d):
+        raise ValueError("out must be uint8 [num_seqs, num_q_heads, head_dim]")
+    code = _dtype_code(kv_dtype)
+    S = num_splits
+    if workspace is None:
+        if S == 0:
+            S = pd_choose_num_splits(B, num_kv_heads, mbs, block_size, sliding_window, d, code,
+                                     q.device.index)
+        workspace = torch.empty(max(pd_decode_workspace_bytes(B, hq, d, S), 16), dtype=torch.uint8,
+                                device=q.device)
+    dev = q.device
+    rc = _lib.pd_decode_e4m3_out(
+        _dev(q, "q", torch.bfloat16, dev), _dev(k_cache, "k_cache", None, dev),
+        _dev(v_cache, "v_cache", None, dev), _dev(block_tables, "block_tables", torch.int32, dev),
+        _dev(seq_lens, "seq_lens", torch.int32, dev), _dev(out, "out", torch.uint8, dev), B,
+        hq, num_kv_heads, d, block_size, mbs, num_blocks, float(scale), S, sliding_window, code,
+        float(k_scale), float(v_scale), float(out_scale), _dev(workspace, "workspace", None, dev),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("pd_decode_e4m3_out", rc)
     return out
 
 
@@ -463,11 +536,12 @@ def pd_decode_balanced_strided(q_rows, k_cache, v_cache, block_tables, plan_dev,
 # ---- paged prefill ---------------------------------------------------------
 def pd_prefill(q, cu_q, k_cache, v_cache, block_tables, seq_lens, out, *, max_q_len,
                num_kv_heads, block_size, num_blocks, scale, causal=True, sliding_window=0,
-               kv_dtype=PD_KV_BF16, k_scale=1.0, v_scale=1.0, stream=None):
+               kv_dtype=PD_KV_BF16, k_scale=1.0, v_scale=1.0, stream=None, crosscheck=False):
     """Paged (chunked) prefill. q and out: contiguous bf16 [total_q, Hq, D];
     cu_q: int32 [B + 1] query-row offsets; seq_lens: int32 [B] keys in the
     cache (new tokens included); max_q_len: host int, the largest q length.
-    pd_prefill_strided takes token rows of a wider buffer instead."""
+    pd_prefill_strided takes token rows of a wider buffer instead.
+    crosscheck: call pd_prefill_crosscheck (the mma.sync kernel)."""
     if q.dim() != 3 or out.dim() != 3:
         raise ValueError("q and out must be bf16 [total_q, num_q_heads, head_dim]")
     T, hq, d = q.shape
@@ -477,7 +551,8 @@ def pd_prefill(q, cu_q, k_cache, v_cache, block_tables, seq_lens, out, *, max_q_
     if tuple(cu_q.shape) != (B + 1,):
         raise ValueError("cu_q must be int32 [num_seqs + 1]")
     dev = q.device
-    rc = _lib.pd_prefill(
+    fn = "pd_prefill_crosscheck" if crosscheck else "pd_prefill"
+    rc = getattr(_lib, fn)(
         _dev(q, "q", torch.bfloat16, dev), 0, _dev(cu_q, "cu_q", torch.int32, dev),
         _dev(k_cache, "k_cache", None, dev), _dev(v_cache, "v_cache", None, dev),
         _dev(block_tables, "block_tables", torch.int32, dev),
@@ -485,14 +560,14 @@ def pd_prefill(q, cu_q, k_cache, v_cache, block_tables, seq_lens, out, *, max_q_
         B, int(max_q_len), hq, num_kv_heads, d, block_size, block_tables.shape[1], num_blocks,
         float(scale), int(bool(causal)), int(sliding_window), _dtype_code(kv_dtype),
         float(k_scale), float(v_scale), _stream(stream))
-    _check("pd_prefill", rc)
+    _check(fn, rc)
     return out
 
 
 def pd_prefill_strided(q_rows, cu_q, k_cache, v_cache, block_tables, seq_lens, out_rows, *,
                        num_q_heads, head_dim, max_q_len, num_kv_heads, block_size, num_blocks,
                        scale, causal=True, sliding_window=0, kv_dtype=PD_KV_BF16, k_scale=1.0,
-                       v_scale=1.0, stream=None):
+                       v_scale=1.0, stream=None, crosscheck=False):
     """pd_prefill with token rows of a wider buffer: q_rows / out_rows are
     contiguous bf16 [total_q, row] tensors holding each token's Hq * D
     values in the first Hq * D of its row (fused QKV rows, padded outputs)."""
@@ -502,7 +577,8 @@ def pd_prefill_strided(q_rows, cu_q, k_cache, v_cache, block_tables, seq_lens, o
         raise ValueError("q_rows and out_rows have different numbers of rows")
     B = int(seq_lens.shape[0])
     dev = q_rows.device
-    rc = _lib.pd_prefill(
+    fn = "pd_prefill_crosscheck" if crosscheck else "pd_prefill"
+    rc = getattr(_lib, fn)(
         _dev(q_rows, "q_rows", torch.bfloat16, dev), stride, _dev(cu_q, "cu_q", torch.int32, dev),
         _dev(k_cache, "k_cache", None, dev), _dev(v_cache, "v_cache", None, dev),
         _dev(block_tables, "block_tables", torch.int32, dev),
@@ -511,5 +587,5 @@ def pd_prefill_strided(q_rows, cu_q, k_cache, v_cache, block_tables, seq_lens, o
         num_q_heads, num_kv_heads, head_dim, block_size, block_tables.shape[1], num_blocks,
         float(scale), int(bool(causal)), int(sliding_window), _dtype_code(kv_dtype),
         float(k_scale), float(v_scale), _stream(stream))
-    _check("pd_prefill_strided", rc)
+    _check(fn, rc)
     return out_rows

@@ -150,7 +150,44 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// FP8 calibration scales from absmax values: absmax / 448 with IEEE fp32
+// division, 1 where the absmax is not positive (an all-zero tensor, or NaN).
+__global__ void fp8_scales_kernel(const float* __restrict__ absmax, float* __restrict__ scales,
+                                  int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) {
+    const float a = absmax[i];
+    scales[i] = a > 0.0f ? __fdiv_rn(a, 448.0f) : 1.0f;
+  }
+}
+
+// The cache write's own encoders applied to fp32 bit patterns first + i
+// (i < n): format 0 = E4M3, 1 = E2M1 (one code per byte).
+__global__ void encode_bits_kernel(int format, uint32_t first, int64_t n, uint8_t* __restrict__ out) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += stride) {
+    const float x = __uint_as_float(first + static_cast<uint32_t>(i));
+    out[i] = static_cast<uint8_t>(format == 0 ? e4m3_encode(x) : e2m1_encode(x));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_fp8_scales(const float* absmax, float* scales, int n, cudaStream_t st) {
+  fp8_scales_kernel<<<(n + 255) / 256, 256, 0, st>>>(absmax, scales, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_encode_bits(int format, uint32_t first, int64_t n, uint8_t* out, int num_sms,
+                               cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  encode_bits_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(format, first, n, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_reshape_and_cache(const uint16_t* key, const uint16_t* value, uint8_t* kc,
                                      uint8_t* vc, const int32_t* slots, int T, int hkv, int d,

@@ -23,7 +23,9 @@
 //    they hand back afterwards, and write the piece's partial or output row.
 //  * Every consumer barrier is an mbarrier with a bounded wait, and every
 //    wait gives up after ~2 s with a device status bit, so a stalled CTA
-//    ends with an error instead of hanging.
+//    ends with an error instead of hanging. A warp that gives up raises the
+//    CTA's abort word, which every other wait polls; the producer then issues
+//    nothing more and waits for the copies it already issued before leaving.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -112,6 +114,11 @@ struct Cfg {
   // per copy and cache: bytes landed by TMA
   static constexpr uint32_t kCopyBytes =
       kBR * kRowBytes + (FMT == PD_KV_NVFP4 ? kBR * (D / 16) : 0);
+  // NVFP4 with 16-row pages and 64-key stages: one gather of the stage's four
+  // pages per cache and section (data slab, scale slab) instead of four bulk
+  // copies each, so a 9 KB stage takes 4 copy operations instead of 16
+  static constexpr bool kGather = FMT == PD_KV_NVFP4 && BS == 16 && kDSplit == 1;
+  static_assert(!kGather || kNCopy == 4, "a gather covers exactly four pages");
   // dynamic shared memory for a GQA group of G heads (q slots of G rows),
   // with 1 KB of slack for aligning the ring to 1024 bytes
   static constexpr int smem_bytes(int G) { return kQOffset + kQSlots * G * D * 2 + 1024; }
@@ -152,7 +159,9 @@ struct ConsumerSync {
 template <int FMT, int D, int NT, int BS>
 __global__ void __launch_bounds__(kMmaThreads)
     partial_balanced_kernel(const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_ks,
+                       const __grid_constant__ CUtensorMap tm_vs, const DecodeArgs a) {
   using C = Cfg<FMT, D, NT, BS>;
   constexpr bool F16 = C::kF16;
   // let the dependent combine grid be scheduled as this grid drains (it waits
@@ -196,10 +205,14 @@ __global__ void __launch_bounds__(kMmaThreads)
     *abort_s = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if constexpr (FMT != PD_KV_NVFP4) {
+  if constexpr (FMT != PD_KV_NVFP4 || C::kGather) {
     if (tid == kConsumerWarps * 32) {  // the tensor maps are kernel parameters
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
+      if constexpr (C::kGather) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_ks)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_vs)) : "memory");
+      }
     }
   }
   __syncthreads();
@@ -288,6 +301,9 @@ __global__ void __launch_bounds__(kMmaThreads)
               }
             }
           }
+          if constexpr (C::kGather) {
+            if (bytes != 0) bytes = 2u * C::kNCopy * C::kCopyBytes;  // pages past the pool land zeros
+          }
           if (j == 0) bytes += q_bytes;
           const uint32_t fb = smem_u32(&full_bar[st]);
           if (lane == 0) {
@@ -310,7 +326,14 @@ __global__ void __launch_bounds__(kMmaThreads)
             const uint16_t* qsrc = a.q + static_cast<int64_t>(b) * a.q_stride + g * G * D;
             bulk_load(smem_u32(qslots + qslot * q_bytes), qsrc, q_bytes, fb);
           }
-          {
+          if constexpr (C::kGather) {
+            if (bytes > (j == 0 ? q_bytes : 0u)) {
+              const uint32_t kst = smem_u32(ring + st * C::kStageBytes);
+              issue_nvfp4_gather<D>(lane, kst, kst + C::kCacheStageBytes, C::kDataBytes, &tm_k,
+                                    &tm_v, &tm_ks, &tm_vs, g, a.data_bytes, pages,
+                                    static_cast<int>(a.num_blocks), fb);
+            }
+          } else {
             int my_page = -1;
 #pragma unroll
             for (int jj = 0; jj < C::kNCopy; ++jj)
@@ -365,10 +388,11 @@ __global__ void __launch_bounds__(kMmaThreads)
     if (!ok) {
       if (lane == 0) atomicOr(a.flags, PD_DEV_TIMEOUT);
       *abort_s = 1;
-      // let the copies already issued land before the block can exit
-      for (int t = max(0, i - C::kStages); t < i; ++t)
-        (void)mbar_wait(smem_u32(&full_bar[t % C::kStages]), (t / C::kStages) & 1);
     }
+    // every copy issued lands before the block can exit (consumers that gave
+    // up no longer wait for them)
+    for (int t = max(0, i - C::kStages); t < i; ++t)
+      (void)mbar_wait(smem_u32(&full_bar[t % C::kStages]), (t / C::kStages) & 1);
     return;
   }
 
@@ -390,11 +414,14 @@ __global__ void __launch_bounds__(kMmaThreads)
   while (!aborted) {
     int st = i % C::kStages;
     {
-      bool ok = warp_wait(smem_u32(&full_bar[st]), (i / C::kStages) & 1, abort_s);
+      bool ok = warp_wait(smem_u32(&full_bar[st]), (i / C::kStages) & 1, abort_s,
+                          a.consumer_wait_ns);
       // head_dim split: the warps meet at named barriers every tile, so they
       // must agree on every wait's outcome before reading the stage record
       if constexpr (C::kDSplit == 4) ok = consumers_vote(ok);
       if (!ok) {
+        if (lane == 0) atomicOr(a.flags, PD_DEV_TIMEOUT);
+        *abort_s = 1;
         aborted = true;
         break;
       }
@@ -440,9 +467,12 @@ __global__ void __launch_bounds__(kMmaThreads)
     if (last || aborted) break;
     st = i % C::kStages;
     {
-      bool ok = warp_wait(smem_u32(&full_bar[st]), (i / C::kStages) & 1, abort_s);
+      bool ok = warp_wait(smem_u32(&full_bar[st]), (i / C::kStages) & 1, abort_s,
+                          a.consumer_wait_ns);
       if constexpr (C::kDSplit == 4) ok = consumers_vote(ok);
       if (!ok) {
+        if (lane == 0) atomicOr(a.flags, PD_DEV_TIMEOUT);
+        *abort_s = 1;
         aborted = true;
         break;
       }
@@ -627,15 +657,26 @@ template <int FMT, int D, int NT, int BS>
 cudaError_t launch_bal_cfg(const DecodeArgs& a, cudaStream_t st) {
   using C = Cfg<FMT, D, NT, BS>;
   const int smem = C::smem_bytes(a.group);
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, tks, tvs;
   std::memset(&tk, 0, sizeof(tk));
   std::memset(&tv, 0, sizeof(tv));
+  std::memset(&tks, 0, sizeof(tks));
+  std::memset(&tvs, 0, sizeof(tvs));
   if constexpr (FMT != PD_KV_NVFP4) {
     const int64_t rows = a.num_blocks * a.block_size;
     if (!encode_cache_map(&tk, a.k_cache, FMT, D, a.num_kv_heads, rows, C::kCopyElems, C::kBR,
                           C::kSwizzle) ||
         !encode_cache_map(&tv, a.v_cache, FMT, D, a.num_kv_heads, rows, C::kCopyElems, C::kBR,
                           C::kSwizzle))
+      return cudaErrorInvalidValue;
+  } else if constexpr (C::kGather) {
+    // page gathers: data slabs ([16][D/2] bytes of a head) and scale slabs
+    // ([16][D/16]) of whole pages
+    constexpr int kSlab = 16 * (D / 2), kScales = 16 * (D / 16);
+    if (!encode_nvfp4_gather_map(&tk, a.k_cache, a.page_bytes, a.num_blocks, kSlab) ||
+        !encode_nvfp4_gather_map(&tv, a.v_cache, a.page_bytes, a.num_blocks, kSlab) ||
+        !encode_nvfp4_gather_map(&tks, a.k_cache, a.page_bytes, a.num_blocks, kScales) ||
+        !encode_nvfp4_gather_map(&tvs, a.v_cache, a.page_bytes, a.num_blocks, kScales))
       return cudaErrorInvalidValue;
   }
   auto kern = partial_balanced_kernel<FMT, D, NT, BS>;
@@ -668,7 +709,7 @@ cudaError_t launch_bal_cfg(const DecodeArgs& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tk, tv, a);
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, tks, tvs, a);
 }
 
 template <int FMT, int D, int NT>

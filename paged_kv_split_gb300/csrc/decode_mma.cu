@@ -93,16 +93,24 @@ struct Cfg {
   static_assert(kMergeBytes <= kRingBytes, "the end-of-CTA merge reuses the ring");
   static constexpr int kQMaxBytes = kDSplit == 4 ? 2 * 4 * 8 * 4 : 0;  // [NT][warp][8] floats
   static constexpr int kBarOffset = kRingBytes + kRedBytes + kQMaxBytes;
-  static constexpr int kSmemBytes = kBarOffset + 2 * kStages * 8 + kStages * 4 + 1024;
+  // full[kStages], empty[kStages], the stages' bad-copy masks, the abort word
+  static constexpr int kSmemBytes = kBarOffset + 2 * kStages * 8 + kStages * 4 + 16 + 1024;
   // per copy and cache: bytes landed by TMA
   static constexpr uint32_t kCopyBytes =
       kBR * kRowBytes + (FMT == PD_KV_NVFP4 ? kBR * (D / 16) : 0);
+  // NVFP4 with 16-row pages and 64-key stages: one gather of the stage's four
+  // pages per cache and section (data slab, scale slab) instead of four bulk
+  // copies each, so a 9 KB stage takes 4 copy operations instead of 16
+  static constexpr bool kGather = FMT == PD_KV_NVFP4 && BS == 16 && kDSplit == 1;
+  static_assert(!kGather || kNCopy == 4, "a gather covers exactly four pages");
 };
 
 template <int FMT, int D, int NT, int BS>
 __global__ void __launch_bounds__(kMmaThreads)
     partial_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_ks,
+                       const __grid_constant__ CUtensorMap tm_vs, const DecodeArgs a) {
   using C = Cfg<FMT, D, NT, BS>;
   constexpr bool F16 = C::kF16;
   // let the dependent combine grid be scheduled as this grid drains (it waits
@@ -129,10 +137,16 @@ __global__ void __launch_bounds__(kMmaThreads)
   const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
   int spec_entry = -1;
   if (warp == kConsumerWarps && a.sliding_window == 0) {
-    if constexpr (FMT != PD_KV_NVFP4) {
+    if constexpr (FMT != PD_KV_NVFP4 || C::kGather) {
       if (lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
+      }
+      if constexpr (C::kGather) {
+        if (lane == 1) {
+          asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_ks)) : "memory");
+          asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_vs)) : "memory");
+        }
       }
     }
     const int e = s * a.chunk + lane;
@@ -175,12 +189,15 @@ __global__ void __launch_bounds__(kMmaThreads)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
   uint64_t* empty_bar = full_bar + C::kStages;
   uint32_t* bad_copies = reinterpret_cast<uint32_t*>(empty_bar + C::kStages);
+  // set by a warp that stops early: the others stop waiting on it
+  volatile int* abort_s = reinterpret_cast<volatile int*>(bad_copies + C::kStages);
 
   if (tid == 0) {
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(smem_u32(&full_bar[i]), 1);
       mbar_init(smem_u32(&empty_bar[i]), kConsumerWarps);
     }
+    *abort_s = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -190,12 +207,16 @@ __global__ void __launch_bounds__(kMmaThreads)
     // entries [cached_base, cached_base + 32) of the block-table row, one per lane
     int cached_base = a.sliding_window == 0 ? s * a.chunk : -(1 << 30);
     int my_entry = spec_entry;
-    for (int i = 0; i < ntiles; ++i) {
+    int i = 0;  // tiles issued
+    for (; i < ntiles; ++i) {
       const int st = i % C::kStages;
+      // a stage is re-armed only after all four consumer warps have handed it
+      // back, which they do only after its previous copies landed
       if (i >= C::kStages &&
-          !mbar_wait(smem_u32(&empty_bar[st]), ((i / C::kStages) - 1) & 1)) {
-        if (lane == 0) atomicOr(a.flags, PD_DEV_TIMEOUT);
-        break;  // consumers give up on their own bounded waits
+          !warp_wait(smem_u32(&empty_bar[st]), ((i / C::kStages) - 1) & 1, abort_s)) {
+        if (lane == 0 && *abort_s == 0) atomicOr(a.flags, PD_DEV_TIMEOUT);
+        *abort_s = 1;
+        break;  // the consumers stopped, or this wait ran out: issue nothing more
       }
       const int t0 = t_base + i * C::kKT;
       uint32_t bad = 0;
@@ -221,6 +242,9 @@ __global__ void __launch_bounds__(kMmaThreads)
           }
         }
       }
+      if constexpr (C::kGather) {
+        if (bytes != 0) bytes = 2u * C::kNCopy * C::kCopyBytes;  // pages past the pool land zeros
+      }
       const uint32_t fb = smem_u32(&full_bar[st]);
       if (lane == 0) {
         if (bad) atomicOr(a.flags, PD_DEV_BAD_PAGE);
@@ -228,8 +252,16 @@ __global__ void __launch_bounds__(kMmaThreads)
         mbar_arrive_expect_tx(fb, bytes);
       }
       __syncwarp();
-      // one lane per page issues that page's copies, in parallel
-      {
+      // one lane per page issues that page's copies, in parallel (NVFP4 with
+      // 16-row pages: four lanes each gather one section of all four pages)
+      if constexpr (C::kGather) {
+        if (bytes != 0) {
+          const uint32_t kst = smem_u32(ring + st * C::kStageBytes);
+          issue_nvfp4_gather<D>(lane, kst, kst + C::kCacheStageBytes, C::kDataBytes, &tm_k, &tm_v,
+                                &tm_ks, &tm_vs, g, a.data_bytes, pages,
+                                static_cast<int>(a.num_blocks), fb);
+        }
+      } else {
         int my_page = -1;
 #pragma unroll
         for (int j = 0; j < C::kNCopy; ++j)
@@ -264,6 +296,10 @@ __global__ void __launch_bounds__(kMmaThreads)
       }
       __syncwarp();
     }
+    // every copy issued lands before the CTA can end (consumers that gave up
+    // no longer wait for them)
+    for (int t = max(0, i - C::kStages); t < i; ++t)
+      (void)mbar_wait(smem_u32(&full_bar[t % C::kStages]), (t / C::kStages) & 1);
     return;
   }
 
@@ -283,10 +319,13 @@ __global__ void __launch_bounds__(kMmaThreads)
   int red_buf = 0;
   for (int i = 0; i < ntiles; ++i) {
     const int st = i % C::kStages;
-    // after one failed wait, stop waiting (bounded total time); results are
-    // then discarded, but every named barrier is still reached
-    if (!failed && !mbar_wait(smem_u32(&full_bar[st]), (i / C::kStages) & 1)) {
+    // after one failed wait, stop waiting (bounded total time) and stop handing
+    // stages back, so that the producer re-arms none whose copies may still be
+    // landing; results are then discarded, but every named barrier is reached
+    if (!failed && !warp_wait(smem_u32(&full_bar[st]), (i / C::kStages) & 1, abort_s,
+                              a.consumer_wait_ns)) {
       if (lane == 0) atomicOr(a.flags, PD_DEV_TIMEOUT);
+      *abort_s = 1;
       failed = true;
     }
     const uint32_t kst = smem_u32(ring + st * C::kStageBytes);
@@ -297,7 +336,7 @@ __global__ void __launch_bounds__(kMmaThreads)
     consume_tile<FMT, D, NT>(ts, StageView{kst, vst, t0, t_begin, t_end, bad}, tp, red, red_buf);
     if constexpr (C::kDSplit == 4) red_buf ^= 1;
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
+    if (lane == 0 && !failed) mbar_arrive(smem_u32(&empty_bar[st]));
   }
 
   // ---- finish: full row sums, then write (O / l, m, l) ----
@@ -400,15 +439,26 @@ __global__ void __launch_bounds__(kMmaThreads)
 template <int FMT, int D, int NT, int BS>
 cudaError_t launch_mma_cfg(const DecodeArgs& a, cudaStream_t st) {
   using C = Cfg<FMT, D, NT, BS>;
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, tks, tvs;
   std::memset(&tk, 0, sizeof(tk));
   std::memset(&tv, 0, sizeof(tv));
+  std::memset(&tks, 0, sizeof(tks));
+  std::memset(&tvs, 0, sizeof(tvs));
   if constexpr (FMT != PD_KV_NVFP4) {
     const int64_t rows = a.num_blocks * a.block_size;
     if (!encode_cache_map(&tk, a.k_cache, FMT, D, a.num_kv_heads, rows, C::kCopyElems, C::kBR,
                           C::kSwizzle) ||
         !encode_cache_map(&tv, a.v_cache, FMT, D, a.num_kv_heads, rows, C::kCopyElems, C::kBR,
                           C::kSwizzle))
+      return cudaErrorInvalidValue;
+  } else if constexpr (C::kGather) {
+    // page gathers: data slabs ([16][D/2] bytes of a head) and scale slabs
+    // ([16][D/16]) of whole pages
+    constexpr int kSlab = 16 * (D / 2), kScales = 16 * (D / 16);
+    if (!encode_nvfp4_gather_map(&tk, a.k_cache, a.page_bytes, a.num_blocks, kSlab) ||
+        !encode_nvfp4_gather_map(&tv, a.v_cache, a.page_bytes, a.num_blocks, kSlab) ||
+        !encode_nvfp4_gather_map(&tks, a.k_cache, a.page_bytes, a.num_blocks, kScales) ||
+        !encode_nvfp4_gather_map(&tvs, a.v_cache, a.page_bytes, a.num_blocks, kScales))
       return cudaErrorInvalidValue;
   }
   auto kern = partial_mma_kernel<FMT, D, NT, BS>;
@@ -433,7 +483,7 @@ cudaError_t launch_mma_cfg(const DecodeArgs& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tk, tv, a);
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, tks, tvs, a);
 }
 
 template <int FMT, int D, int NT>

@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kThreads) partial_simple_kernel(const DecodeAr
 // 4 consecutive output elements. The split weights w_s = l_s 2^(m_s - M)
 // are computed once, split-parallel across lanes, into shared memory; the
 // weighted sum over the splits then issues its loads four splits at a time.
-template <int D>
+template <int D, bool E4M3_OUT>
 __global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
   // Launched as a programmatic dependent of the partial kernel: wait until
   // that grid has completed and its workspace writes are visible.
@@ -263,12 +263,23 @@ __global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
     acc.w = fmaf(ws, o.w, acc.w);
   }
   const float inv = 1.0f / fmaxf(wsum, 1e-20f);
-  const uint32_t lo01 = static_cast<uint32_t>(f32_to_bf16(acc.x * inv)) |
-                        (static_cast<uint32_t>(f32_to_bf16(acc.y * inv)) << 16);
-  const uint32_t lo23 = static_cast<uint32_t>(f32_to_bf16(acc.z * inv)) |
-                        (static_cast<uint32_t>(f32_to_bf16(acc.w * inv)) << 16);
-  *reinterpret_cast<uint2*>(a.out + static_cast<int64_t>(b) * a.out_stride + h * D + d) =
-      make_uint2(lo01, lo23);
+  if constexpr (E4M3_OUT) {
+    // E4M3(o / out_scale), IEEE division, the cache encoder's rounding
+    const float s = a.out_scale;
+    const uint32_t w4 = e4m3_encode(__fdiv_rn(acc.x * inv, s)) |
+                        (e4m3_encode(__fdiv_rn(acc.y * inv, s)) << 8) |
+                        (e4m3_encode(__fdiv_rn(acc.z * inv, s)) << 16) |
+                        (e4m3_encode(__fdiv_rn(acc.w * inv, s)) << 24);
+    *reinterpret_cast<uint32_t*>(a.out8 + static_cast<int64_t>(b) * a.out_stride + h * D + d) =
+        w4;
+  } else {
+    const uint32_t lo01 = static_cast<uint32_t>(f32_to_bf16(acc.x * inv)) |
+                          (static_cast<uint32_t>(f32_to_bf16(acc.y * inv)) << 16);
+    const uint32_t lo23 = static_cast<uint32_t>(f32_to_bf16(acc.z * inv)) |
+                          (static_cast<uint32_t>(f32_to_bf16(acc.w * inv)) << 16);
+    *reinterpret_cast<uint2*>(a.out + static_cast<int64_t>(b) * a.out_stride + h * D + d) =
+        make_uint2(lo01, lo23);
+  }
   // Only now let the next step's partial grid be placed: a combine CTA that
   // lingered beside it would hold registers that the partial kernel's third
   // CTA of an SM needs (three balanced BF16 CTAs take 61,440 of the 65,536).
@@ -337,7 +348,8 @@ cudaError_t launch_combine_pdl(const CombineArgs& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel<D>, a);
+  if (a.out8 != nullptr) return cudaLaunchKernelEx(&cfg, combine_kernel<D, true>, a);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<D, false>, a);
 }
 
 cudaError_t launch_decode_combine(const CombineArgs& a, int head_dim, cudaStream_t st) {

@@ -60,17 +60,44 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking probe of the same phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Wait for the phase with the given parity to complete; false after ~2 s.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false after limit_ns
+// (default ~2 s).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+// The same wait, which also gives up as soon as `abort_flag` (a shared-memory
+// word another warp of the CTA sets when it stops) is non-zero. A limit of 0
+// makes it a single non-blocking probe (a test's way to make waits run out).
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity,
+                                                   const volatile int* abort_flag,
+                                                   uint64_t limit_ns = kWaitLimitNs) {
+  if (limit_ns == 0) return mbar_test_wait(bar, parity);
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag != 0 || global_ns() - t0 > limit_ns) return false;
   }
   return true;
 }
@@ -78,9 +105,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 // (false if any lane ran out of time or `abort_flag` is set), so that the
 // warp never splits on a wait that ends near its limit.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
-                                          const volatile int* abort_flag) {
-  (void)abort_flag;
-  return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity));
+                                          const volatile int* abort_flag,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait_or_abort(bar, parity, abort_flag, limit_ns));
 }
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             int z, uint32_t bar) {
@@ -89,6 +116,46 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
+}
+// Four rows r0..r3 (any order, each may lie outside the tensor: zeros) of a
+// 2-D tensor map whose box is one row high, from column x, landing one after
+// another at dst.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int r0,
+                                            int r1, int r2, int r3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+// One NVFP4 stage of four 16-row pages for kv head g, by four lanes: lane 0
+// gathers the K data slabs, 1 the V data slabs, 2 the K scale slabs, 3 the V
+// scale slabs (maps as from encode_nvfp4_gather_map). pages[j] < 0 (no copy:
+// outside the pool or past the key range) reads row oob_row, past the pool:
+// zeros, with the same byte count. Lands as four pages of [16][D/2] data at
+// kst / vst and four of [16][D/16] scales at + data_bytes_in_stage.
+template <int D>
+__device__ __forceinline__ void issue_nvfp4_gather(int lane, uint32_t kst, uint32_t vst,
+                                                   uint32_t data_bytes_in_stage,
+                                                   const CUtensorMap* tm_kd,
+                                                   const CUtensorMap* tm_vd,
+                                                   const CUtensorMap* tm_ks,
+                                                   const CUtensorMap* tm_vs, int g,
+                                                   int64_t page_data_bytes, const int* pages,
+                                                   int oob_row, uint32_t bar) {
+  constexpr int kSlabWords = 16 * (D / 2) / 4;    // a head's data slab in one page
+  constexpr int kScaleWords = 16 * (D / 16) / 4;  // its scale slab
+  if (lane >= 4) return;
+  const int r0 = pages[0] >= 0 ? pages[0] : oob_row;
+  const int r1 = pages[1] >= 0 ? pages[1] : oob_row;
+  const int r2 = pages[2] >= 0 ? pages[2] : oob_row;
+  const int r3 = pages[3] >= 0 ? pages[3] : oob_row;
+  const bool scales = lane >= 2;
+  const CUtensorMap* m = lane == 0 ? tm_kd : (lane == 1 ? tm_vd : (lane == 2 ? tm_ks : tm_vs));
+  const uint32_t dst = ((lane & 1) ? vst : kst) + (scales ? data_bytes_in_stage : 0u);
+  const int x = scales ? static_cast<int>(page_data_bytes / 4) + g * kScaleWords
+                       : g * kSlabWords;
+  tma_gather4(dst, m, x, r0, r1, r2, r3, bar);
 }
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {
@@ -267,6 +334,28 @@ inline bool encode_cache_map(CUtensorMap* m, const void* base, int kv_dtype, int
                      : (D * esz >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
                                        : CU_TENSOR_MAP_L2_PROMOTION_L2_64B),
       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rc == CUDA_SUCCESS;
+}
+
+// 2-D map over an NVFP4 cache for page gathers: one row per page (row stride
+// = the page stride), 32-bit elements across the page, box = box_bytes of one
+// row. A gather at column x of four pages copies the same box_bytes-long
+// section (a kv head's data slab or its scale slab) of each page.
+inline bool encode_nvfp4_gather_map(CUtensorMap* m, const void* base, int64_t page_bytes,
+                                    int64_t num_pages, int box_bytes) {
+  auto fn = encode_fn();
+  if (!fn || page_bytes % 16 != 0 || box_bytes % 16 != 0 || box_bytes / 4 > 256) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(page_bytes / 4),
+                              static_cast<cuuint64_t>(num_pages)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(page_bytes)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes / 4), 1u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult rc = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE,
+                         box_bytes >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                          : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return rc == CUDA_SUCCESS;
 }
 

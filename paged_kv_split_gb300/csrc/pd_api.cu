@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <functional>
 #include <mutex>
 #include <vector>
@@ -28,6 +29,11 @@ struct DeviceInfo {
   cudaError_t err = cudaSuccess;
 };
 DeviceInfo g_devices[kMaxDevices];
+
+// Limit of the decode kernels' consumer-side waits (ns). Only a test changes
+// it (pd_test_set_consumer_wait_ns), to make those waits run out on purpose.
+constexpr uint32_t kDefaultConsumerWaitNs = 2000000000u;
+std::atomic<uint32_t> g_consumer_wait_ns{kDefaultConsumerWaitNs};
 
 // SM count and status-word address of the current device (looked up once).
 cudaError_t current_device(DeviceInfo** out) {
@@ -57,10 +63,9 @@ struct DecodeShape {
   int64_t nb;
 };
 
-// Shared checks of pd_decode / pd_decode_partial (S already resolved).
-int check_decode(const DecodeShape& s, const void* q, const void* kc, const void* vc,
-                 const int32_t* bt, const int32_t* lens, float k_scale, float v_scale,
-                 const void* ws, size_t ws_bytes) {
+// Shape and scale checks of every decode call (no pointer, split count or
+// workspace involved), in the order the status codes are reported.
+int check_decode_shape(const DecodeShape& s, float k_scale, float v_scale) {
   if (s.B < 0 || s.B > 65535) return PD_ERR_INVALID_ARG;
   if (s.Hkv <= 0 || s.Hq <= 0 || s.Hq % s.Hkv != 0) return PD_ERR_INVALID_ARG;
   if (s.Hq / s.Hkv > kMaxGroup) return PD_ERR_UNSUPPORTED;
@@ -69,9 +74,18 @@ int check_decode(const DecodeShape& s, const void* q, const void* kc, const void
   if (s.mbs <= 0 || s.nb <= 0 || s.W < 0) return PD_ERR_INVALID_ARG;
   if (static_cast<int64_t>(s.mbs) * s.bs > (int64_t{1} << 30)) return PD_ERR_INVALID_ARG;
   if (s.nb * s.bs > INT32_MAX) return PD_ERR_INVALID_ARG;  // pool rows are int32 coordinates
-  if (s.S < 1 || s.S > kMaxSplits) return PD_ERR_INVALID_ARG;
   if (s.kv_dtype == PD_KV_FP8_E4M3 && !(scale_ok(k_scale) && scale_ok(v_scale)))
     return PD_ERR_INVALID_ARG;
+  return PD_OK;
+}
+
+// Shared checks of pd_decode / pd_decode_partial (S already resolved).
+int check_decode(const DecodeShape& s, const void* q, const void* kc, const void* vc,
+                 const int32_t* bt, const int32_t* lens, float k_scale, float v_scale,
+                 const void* ws, size_t ws_bytes) {
+  const int rc = check_decode_shape(s, k_scale, v_scale);
+  if (rc != PD_OK) return rc;
+  if (s.S < 1 || s.S > kMaxSplits) return PD_ERR_INVALID_ARG;
   if (s.B == 0) return PD_OK;
   if (!dev_ptr_ok(q) || !dev_ptr_ok(kc) || !dev_ptr_ok(vc) || !dev_ptr_ok(bt) ||
       !dev_ptr_ok(lens) || !dev_ptr_ok(ws))
@@ -115,6 +129,7 @@ DecodeArgs make_decode_args(const DecodeShape& s, const void* q, const void* kc,
   a.scale_log2 = scale * kLog2e;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
+  a.consumer_wait_ns = g_consumer_wait_ns.load(std::memory_order_relaxed);
   return a;
 }
 
@@ -136,6 +151,8 @@ CombineArgs make_combine_args(int B, int Hq, int D, int bs, int mbs, int S, int 
   c.skip_direct = 0;
   c.plan_seg = nullptr;
   c.num_kv_heads = 0;
+  c.out8 = nullptr;
+  c.out_scale = 1.0f;
   return c;
 }
 
@@ -373,25 +390,37 @@ bool q_stride_ok(int64_t q_stride, int Hq, int D) {
   return q_stride == 0 || (q_stride >= static_cast<int64_t>(Hq) * D && q_stride % 8 == 0);
 }
 
-// The tensor-core partial kernel runs by default; PD_PARTIAL_KERNEL=simple
-// selects the CUDA-core kernel instead (kept as an independent cross-check).
-bool use_simple_partial() {
-  static const bool simple = [] {
-    const char* v = getenv("PD_PARTIAL_KERNEL");
-    return v != nullptr && strcmp(v, "simple") == 0;
-  }();
-  return simple;
-}
-
-// The tcgen05 prefill kernel runs by default; PD_PREFILL_KERNEL=mma selects
-// the mma.sync kernel instead (kept as an independent cross-check). Read on
-// every call, so that one process can run both.
-bool use_mma_sync_prefill() {
-  const char* v = getenv("PD_PREFILL_KERNEL");
-  return v != nullptr && strcmp(v, "mma") == 0;
-}
-
 }  // namespace
+
+int decode_checks(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* seq_lens, const void* out,
+                  int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t block_size, int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
+                  int32_t num_splits, int32_t sliding_window, int32_t kv_dtype, float k_scale,
+                  float v_scale, int64_t q_stride, int64_t out_stride, int* num_splits_out) {
+  if (!q_stride_ok(q_stride, num_q_heads, head_dim)) return PD_ERR_INVALID_ARG;
+  if (!q_stride_ok(out_stride, num_q_heads, head_dim)) return PD_ERR_INVALID_ARG;
+  if (num_splits < 0 || num_splits > kMaxSplits) return PD_ERR_INVALID_ARG;
+  // shapes first, so that a malformed request is refused before any CUDA call
+  const DecodeShape sh{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       max_blocks_per_seq, 1, sliding_window, kv_dtype, num_blocks};
+  const int rc = check_decode_shape(sh, k_scale, v_scale);
+  if (rc != PD_OK) return rc;
+  if (!isfinite(scale)) return PD_ERR_INVALID_ARG;
+  if (num_seqs > 0 && (!dev_ptr_ok(q) || !dev_ptr_ok(k_cache) || !dev_ptr_ok(v_cache) ||
+                       !dev_ptr_ok(block_tables) || !dev_ptr_ok(seq_lens) || !dev_ptr_ok(out)))
+    return PD_ERR_INVALID_ARG;
+  int S = num_splits;
+  if (S == 0) {
+    DeviceInfo* dev = nullptr;
+    if (current_device(&dev) != cudaSuccess) return PD_ERR_CUDA;
+    S = plan_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, sliding_window,
+                    dev->num_sms, mma_ctas_per_sm_estimate(kv_dtype, head_dim));
+  }
+  *num_splits_out = S;
+  return PD_OK;
+}
+
 }  // namespace pd
 
 using namespace pd;
@@ -506,7 +535,8 @@ int partial_impl(const void* q, const void* k_cache, const void* v_cache,
                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                  int32_t max_blocks_per_seq, int64_t num_blocks, float scale, int32_t num_splits,
                  int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
-                 void* workspace, size_t workspace_bytes, void* stream, int64_t q_stride) {
+                 void* workspace, size_t workspace_bytes, void* stream, int64_t q_stride,
+                 bool cuda_core = false) {
   const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                       max_blocks_per_seq, num_splits, sliding_window, kv_dtype, num_blocks};
   const int rc = check_decode(s, q, k_cache, v_cache, block_tables, seq_lens, k_scale, v_scale,
@@ -520,8 +550,8 @@ int partial_impl(const void* q, const void* k_cache, const void* v_cache,
   if (!q_stride_ok(q_stride, num_q_heads, head_dim)) return PD_ERR_INVALID_ARG;
   if (q_stride) a.q_stride = q_stride;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return cuda_status(use_simple_partial() ? launch_decode_partial(a, head_dim, kv_dtype, st)
-                                          : launch_decode_partial_mma(a, head_dim, kv_dtype, st));
+  return cuda_status(cuda_core ? launch_decode_partial(a, head_dim, kv_dtype, st)
+                               : launch_decode_partial_mma(a, head_dim, kv_dtype, st));
 }
 }  // namespace
 
@@ -568,57 +598,52 @@ int decode_split(const void* q, const void* k_cache, const void* v_cache,
                  int32_t block_size, int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
                  int32_t num_splits, int32_t sliding_window, int32_t kv_dtype, float k_scale,
                  float v_scale, void* workspace, size_t workspace_bytes, void* stream,
-                 int64_t q_stride, int64_t out_stride = 0) {
-  if (!q_stride_ok(q_stride, num_q_heads, head_dim)) return PD_ERR_INVALID_ARG;
-  if (!q_stride_ok(out_stride, num_q_heads, head_dim)) return PD_ERR_INVALID_ARG;
-  if (num_splits < 0 || num_splits > kMaxSplits) return PD_ERR_INVALID_ARG;
-  if (num_seqs > 0 && !dev_ptr_ok(out)) return PD_ERR_INVALID_ARG;
-  int S = num_splits;
-  if (S == 0) {
-    DeviceInfo* dev = nullptr;
-    if (current_device(&dev) != cudaSuccess) return PD_ERR_CUDA;
-    if (num_kv_heads <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 || sliding_window < 0)
-      return PD_ERR_INVALID_ARG;
-    if (!head_dim_ok(head_dim) || !dtype_ok(kv_dtype)) return PD_ERR_UNSUPPORTED;
-    S = plan_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size, sliding_window,
-                    dev->num_sms, mma_ctas_per_sm_estimate(kv_dtype, head_dim));
-  }
-  if (use_simple_partial()) {
-    int rc = partial_impl(q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_q_heads,
-                          num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
-                          scale, S, sliding_window, kv_dtype, k_scale, v_scale, workspace,
-                          workspace_bytes, stream, q_stride);
-    if (rc != PD_OK || num_seqs == 0) return rc;
-    if (!dev_ptr_ok(out)) return PD_ERR_INVALID_ARG;
-    CombineArgs c = make_combine_args(num_seqs, num_q_heads, head_dim, block_size,
-                                      max_blocks_per_seq, S, sliding_window, workspace, seq_lens,
-                                      out);
-    if (out_stride) c.out_stride = out_stride;
-    return cuda_status(launch_decode_combine(c, head_dim, static_cast<cudaStream_t>(stream)));
-  }
-  // the partial kernel writes the rows of sequences whose keys fit one split
-  // (and zero rows for empty ones); the combine merges the rest
-  const DecodeShape sh{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                       max_blocks_per_seq, S, sliding_window, kv_dtype, num_blocks};
-  const int rc = check_decode(sh, q, k_cache, v_cache, block_tables, seq_lens, k_scale, v_scale,
-                              workspace, workspace_bytes);
+                 int64_t q_stride, int64_t out_stride = 0, bool cuda_core = false,
+                 float e4m3_out_scale = 0.0f) {
+  int S = 0;
+  const int rc = decode_checks(q, k_cache, v_cache, block_tables, seq_lens, out, num_seqs,
+                               num_q_heads, num_kv_heads, head_dim, block_size,
+                               max_blocks_per_seq, num_blocks, scale, num_splits, sliding_window,
+                               kv_dtype, k_scale, v_scale, q_stride, out_stride, &S);
   if (rc != PD_OK || num_seqs == 0) return rc;
-  if (!isfinite(scale)) return PD_ERR_INVALID_ARG;
+  if (!dev_ptr_ok(workspace)) return PD_ERR_INVALID_ARG;
+  if (workspace_bytes < ws_total_bytes(num_seqs, num_q_heads, head_dim, S))
+    return PD_ERR_WORKSPACE_TOO_SMALL;
   DeviceInfo* dev = nullptr;
   if (current_device(&dev) != cudaSuccess) return PD_ERR_CUDA;
+  const DecodeShape sh{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       max_blocks_per_seq, S, sliding_window, kv_dtype, num_blocks};
   DecodeArgs a = make_decode_args(sh, q, k_cache, v_cache, block_tables, seq_lens, scale, k_scale,
                                   v_scale, workspace, dev->flags);
-  a.out = static_cast<uint16_t*>(out);
-  a.direct = 1;
   if (q_stride) a.q_stride = q_stride;
   if (out_stride) a.out_stride = out_stride;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (launch_decode_partial_mma(a, head_dim, kv_dtype, st) != cudaSuccess) return PD_ERR_CUDA;
   CombineArgs c = make_combine_args(num_seqs, num_q_heads, head_dim, block_size,
                                     max_blocks_per_seq, S, sliding_window, workspace, seq_lens,
                                     out);
-  c.skip_direct = 1;
   if (out_stride) c.out_stride = out_stride;
+  if (e4m3_out_scale > 0.0f) {
+    // E4M3 output: every sequence's partials go through the workspace and the
+    // combine writes the codes
+    c.out = nullptr;
+    c.out8 = static_cast<uint8_t*>(out);
+    c.out_scale = e4m3_out_scale;
+    const cudaError_t e = cuda_core ? launch_decode_partial(a, head_dim, kv_dtype, st)
+                                    : launch_decode_partial_mma(a, head_dim, kv_dtype, st);
+    if (e != cudaSuccess) return PD_ERR_CUDA;
+    return cuda_status(launch_decode_combine(c, head_dim, st));
+  }
+  if (cuda_core) {
+    // the CUDA-core cross-check kernel writes every partial; the combine merges all
+    if (launch_decode_partial(a, head_dim, kv_dtype, st) != cudaSuccess) return PD_ERR_CUDA;
+    return cuda_status(launch_decode_combine(c, head_dim, st));
+  }
+  // the partial kernel writes the rows of sequences whose keys fit one split
+  // (and zero rows for empty ones); the combine merges the rest
+  a.out = static_cast<uint16_t*>(out);
+  a.direct = 1;
+  if (launch_decode_partial_mma(a, head_dim, kv_dtype, st) != cudaSuccess) return PD_ERR_CUDA;
+  c.skip_direct = 1;
   return cuda_status(launch_decode_combine(c, head_dim, st));
 }
 }  // namespace
@@ -822,13 +847,16 @@ int pd_decode_balanced_combine(const void* q, const void* k_cache, const void* v
                          num_pieces, workspace, workspace_bytes, stream, false, true);
 }
 
-int pd_prefill(const void* q, int64_t q_stride, const int32_t* cu_q, const void* k_cache,
-               const void* v_cache, const int32_t* block_tables, const int32_t* seq_lens,
-               void* out, int64_t out_stride, int32_t num_seqs, int32_t max_q_len,
-               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-               int32_t max_blocks_per_seq, int64_t num_blocks, float scale, int32_t causal,
-               int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
-               void* stream) {
+}  // extern "C"
+
+namespace {
+int prefill_impl(const void* q, int64_t q_stride, const int32_t* cu_q, const void* k_cache,
+                 const void* v_cache, const int32_t* block_tables, const int32_t* seq_lens,
+                 void* out, int64_t out_stride, int32_t num_seqs, int32_t max_q_len,
+                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                 int32_t max_blocks_per_seq, int64_t num_blocks, float scale, int32_t causal,
+                 int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
+                 void* stream, bool mma_sync) {
   (void)k_scale;
   (void)v_scale;
   if (num_seqs < 0 || num_seqs > 65535 || max_q_len < 0) return PD_ERR_INVALID_ARG;
@@ -872,12 +900,80 @@ int pd_prefill(const void* q, int64_t q_stride, const int32_t* cu_q, const void*
   a.sliding_window = sliding_window;
   a.scale_log2 = scale * kLog2e;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (use_mma_sync_prefill()) {
+  if (mma_sync) {
     a.tokens_per_cta = 64 / G;
     return cuda_status(launch_prefill(a, k_cache, v_cache, head_dim, max_q_len, st));
   }
   a.tokens_per_cta = 128 / G;
   return cuda_status(launch_prefill_umma(a, k_cache, v_cache, head_dim, max_q_len, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+int pd_prefill(const void* q, int64_t q_stride, const int32_t* cu_q, const void* k_cache,
+               const void* v_cache, const int32_t* block_tables, const int32_t* seq_lens,
+               void* out, int64_t out_stride, int32_t num_seqs, int32_t max_q_len,
+               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+               int32_t max_blocks_per_seq, int64_t num_blocks, float scale, int32_t causal,
+               int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
+               void* stream) {
+  return prefill_impl(q, q_stride, cu_q, k_cache, v_cache, block_tables, seq_lens, out,
+                      out_stride, num_seqs, max_q_len, num_q_heads, num_kv_heads, head_dim,
+                      block_size, max_blocks_per_seq, num_blocks, scale, causal, sliding_window,
+                      kv_dtype, k_scale, v_scale, stream, false);
+}
+
+int pd_prefill_crosscheck(const void* q, int64_t q_stride, const int32_t* cu_q,
+                          const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                          const int32_t* seq_lens, void* out, int64_t out_stride,
+                          int32_t num_seqs, int32_t max_q_len, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                          int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
+                          int32_t causal, int32_t sliding_window, int32_t kv_dtype,
+                          float k_scale, float v_scale, void* stream) {
+  return prefill_impl(q, q_stride, cu_q, k_cache, v_cache, block_tables, seq_lens, out,
+                      out_stride, num_seqs, max_q_len, num_q_heads, num_kv_heads, head_dim,
+                      block_size, max_blocks_per_seq, num_blocks, scale, causal, sliding_window,
+                      kv_dtype, k_scale, v_scale, stream, true);
+}
+
+int pd_decode_crosscheck(const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, const int32_t* seq_lens, void* out,
+                         int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
+                         int64_t num_blocks, float scale, int32_t num_splits,
+                         int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_split(q, k_cache, v_cache, block_tables, seq_lens, out, num_seqs, num_q_heads,
+                      num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
+                      num_splits, sliding_window, kv_dtype, k_scale, v_scale, workspace,
+                      workspace_bytes, stream, 0, 0, true);
+}
+
+int pd_decode_e4m3_out(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* seq_lens, void* out,
+                       int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
+                       int64_t num_blocks, float scale, int32_t num_splits,
+                       int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
+                       float out_scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!(isfinite(out_scale) && out_scale > 0.0f)) return PD_ERR_INVALID_ARG;
+  return decode_split(q, k_cache, v_cache, block_tables, seq_lens, out, num_seqs, num_q_heads,
+                      num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale,
+                      num_splits, sliding_window, kv_dtype, k_scale, v_scale, workspace,
+                      workspace_bytes, stream, 0, 0, false, out_scale);
+}
+
+float pd_fp8_scale(float absmax) { return absmax > 0.0f ? absmax / 448.0f : 1.0f; }
+
+int pd_fp8_scales_from_absmax(const float* absmax, float* scales, int32_t count, void* stream) {
+  if (count < 0) return PD_ERR_INVALID_ARG;
+  if (count == 0) return PD_OK;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(absmax), o = reinterpret_cast<uintptr_t>(scales);
+  if (absmax == nullptr || scales == nullptr || (a & 3u) || (o & 3u)) return PD_ERR_INVALID_ARG;
+  return cuda_status(launch_fp8_scales(absmax, scales, count, static_cast<cudaStream_t>(stream)));
 }
 
 int pd_device_status(int32_t* flags, int32_t reset) {
@@ -892,6 +988,22 @@ int pd_device_status(int32_t* flags, int32_t reset) {
     if (cudaMemcpyToSymbol(g_device_flags, &zero, sizeof(int)) != cudaSuccess) return PD_ERR_CUDA;
   }
   return PD_OK;
+}
+
+int pd_test_encode(int32_t format, uint32_t first_bits, int64_t count, uint8_t* codes,
+                   void* stream) {
+  if ((format != 0 && format != 1) || count < 0 || count > (int64_t{1} << 32))
+    return PD_ERR_INVALID_ARG;
+  if (count == 0) return PD_OK;
+  if (codes == nullptr) return PD_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if (current_device(&dev) != cudaSuccess) return PD_ERR_CUDA;
+  return cuda_status(launch_encode_bits(format, first_bits, count, codes, dev->num_sms,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+uint32_t pd_test_set_consumer_wait_ns(uint32_t ns) {
+  return g_consumer_wait_ns.exchange(ns == 0xFFFFFFFFu ? kDefaultConsumerWaitNs : ns);
 }
 
 }  // extern "C"

@@ -162,6 +162,9 @@ struct DecodeArgs {
   int plan_num_ctas, plan_num_pieces;
   float scale_log2;              // scale * log2(e)
   float k_scale, v_scale;
+  // limit of the consumer warps' waits for a stage of keys (ns; ~2 s unless a
+  // test shortens it to make the waits run out)
+  uint32_t consumer_wait_ns;
 };
 
 struct CombineArgs {
@@ -177,6 +180,10 @@ struct CombineArgs {
   // (row piece * group + h % group) instead of the S splits
   const int32_t* plan_seg;
   int num_kv_heads;
+  // E4M3 output (pd_decode_e4m3_out): when out8 is set, the combine writes
+  // E4M3(o / out_scale) bytes there (row b at b * out_stride) instead of bf16
+  uint8_t* out8;
+  float out_scale;
 };
 
 // Paged prefill: sequence b's query rows are cu_q[b] .. cu_q[b+1]-1 of q and
@@ -214,12 +221,27 @@ __device__ __forceinline__ int checked_seq_len(const int32_t* seq_lens, int b, i
 
 // Launchers (defined in the kernel translation units).
 namespace pd {
+// pd_decode's argument checks, in the order it reports them, up to (not
+// including) the workspace; a split count of 0 is resolved to the automatic
+// choice on the current device. Defined in pd_api.cu; pd_decode_static_ws
+// uses it so that both calls answer a malformed request with the same code.
+int decode_checks(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* seq_lens, const void* out,
+                  int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t block_size, int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
+                  int32_t num_splits, int32_t sliding_window, int32_t kv_dtype, float k_scale,
+                  float v_scale, int64_t q_stride, int64_t out_stride, int* num_splits_out);
 cudaError_t launch_reshape_and_cache(const uint16_t* key, const uint16_t* value, uint8_t* kc,
                                      uint8_t* vc, const int32_t* slots, int T, int hkv, int d,
                                      int bs, int64_t nb, int kv_dtype, float k_scale,
                                      float v_scale, int* flags, cudaStream_t st);
 cudaError_t launch_absmax(const uint16_t* data, int64_t n, float* out, int num_sms,
                           cudaStream_t st);
+cudaError_t launch_fp8_scales(const float* absmax, float* scales, int n, cudaStream_t st);
+// The cache write's E4M3 (format 0) / E2M1 (format 1) encoders on the fp32 bit
+// patterns first .. first + n - 1 (wrapping), one code byte each (a test hook).
+cudaError_t launch_encode_bits(int format, uint32_t first, int64_t n, uint8_t* out, int num_sms,
+                               cudaStream_t st);
 cudaError_t launch_decode_partial(const DecodeArgs& a, int head_dim, int kv_dtype,
                                   cudaStream_t st);
 cudaError_t launch_decode_partial_mma(const DecodeArgs& a, int head_dim, int kv_dtype,

@@ -58,17 +58,15 @@ extern "C" int pd_decode_static_ws(const void* q, const void* k_cache, const voi
                                    int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
                                    int32_t num_splits, int32_t sliding_window, int32_t kv_dtype,
                                    float k_scale, float v_scale, void* stream) {
-  if (num_splits < 0 || num_splits > 1024 || num_seqs < 0 || num_q_heads <= 0 ||
-      num_kv_heads <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 || sliding_window < 0)
-    return PD_ERR_INVALID_ARG;
-  int S = num_splits;
-  if (S == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return PD_ERR_CUDA;
-    S = pd_choose_num_splits(num_seqs, num_kv_heads, max_blocks_per_seq, block_size,
-                             sliding_window, head_dim, kv_dtype, dev);
-    if (S < 1) return -S;
-  }
+  // pd_decode's own checks, in its order, so that both calls answer a
+  // malformed request with the same status; a split count of 0 is resolved
+  // the way pd_decode resolves it
+  int S = 0;
+  const int rc = pd::decode_checks(q, k_cache, v_cache, block_tables, seq_lens, out, num_seqs,
+                                   num_q_heads, num_kv_heads, head_dim, block_size,
+                                   max_blocks_per_seq, num_blocks, scale, num_splits,
+                                   sliding_window, kv_dtype, k_scale, v_scale, 0, 0, &S);
+  if (rc != PD_OK || num_seqs == 0) return rc;
   // The fixed array bounds the problem size: refuse anything that would not fit.
   if (pd_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, S) >
       static_cast<size_t>(PD_STATIC_WORKSPACE_BYTES))

@@ -8,24 +8,27 @@
 //    rows: 128 / G query tokens times the GQA group's G heads, so every K/V
 //    byte it loads serves the whole group. Tiles run from the last one down
 //    (under causality the last tiles see the most keys).
-//  * Warp 4 (producer) copies 64-key K and V tiles of the kv head into a ring
+//  * Warp 8 (producer) copies 64-key K and V tiles of the kv head into a ring
 //    with 3-D TMA tensor copies (128-byte swizzle), one block-table lookup per
 //    page; copies it skips (pages outside the pool, rows past the CTA's keys)
 //    are issued at a row past the pool, which TMA fills with zeros.
-//  * Warp 5 allocates 256 TMEM columns and one of its threads issues the MMAs:
+//  * Warp 9 allocates 256 TMEM columns and one of its threads issues the MMAs:
 //    S_j = Q K_j^T (M = 128 rows, N = 64 keys, K = head_dim; Q and K K-major in
 //    shared memory) into one of two TMEM buffers, so S_{j+1} runs while the
 //    softmax of tile j does; O += P_j V_j (N = head_dim; P K-major in shared
 //    memory, V MN-major straight from the stage) into a TMEM accumulator.
 //    tcgen05.commit signals each result on an mbarrier.
-//  * Warps 0-3: thread m owns row m (TMEM lane m). Per tile it reads its 64
-//    scores with tcgen05.ld, masks (causal position, window, pages outside the
-//    pool), runs one online-softmax step in registers (no shuffles), writes
-//    P as bf16 into the swizzled A-operand tile, and rescales its O row in TMEM
-//    only when its tile max passes the reference max by more than 2^8 (P stays
+//  * Warps 0-7 run the softmax, two threads per row: warp w owns rows
+//    32 (w % 4) .. +31 (TMEM lanes of its warp's quarter) and key half w / 4
+//    of each 64-key tile. Per tile a thread reads its 32 scores with
+//    tcgen05.ld, masks them (causal position, window, pages outside the pool)
+//    with one 32-bit valid-key word, swaps its half-row max with its partner
+//    through shared memory (one named barrier per tile), writes its P slice
+//    as bf16 into the swizzled A-operand tile, and the pair rescales O in TMEM
+//    only when the tile max passes the reference max by more than 2^8 (P stays
 //    <= 256; the result is the same up to rounding). V rows of keys no row of
 //    the CTA may read are zeroed first, so stale stage bytes never meet a zero
-//    weight.
+//    weight. The epilogue adds the two partial row sums and writes O / l.
 //  * Every mbarrier wait is bounded (2 s): on time-out the CTA raises
 //    PD_DEV_TIMEOUT, stops issuing work, waits (bounded) for what it issued,
 //    frees its TMEM and exits.

@@ -192,3 +192,62 @@ def test_prefill_validation(pdlib):
     assert call(q=0x1004) == 1            # misaligned pointer
     assert call(cu=0) == 1                # null pointer
     assert call(sc=float("inf")) == 1
+
+
+def _decode_entry(L, name, **kw):
+    """pd_decode (workspace arguments) or pd_decode_static_ws (none) with
+    placeholder pointers: only argument checks may run."""
+    args = dict(q=0x1000, k=0x2000, v=0x3000, bt=0x4000, lens=0x5000, out=0x7000, B=2, Hq=8,
+                Hkv=2, D=128, bs=16, mbs=4, nb=8, scale=0.1, S=0, W=0, dt=0, ks=1.0, vs=1.0)
+    args.update(kw)
+    a = args
+    P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    head = [a["q"], a["k"], a["v"], a["bt"], a["lens"], a["out"], a["B"], a["Hq"], a["Hkv"],
+            a["D"], a["bs"], a["mbs"], a["nb"], a["scale"], a["S"], a["W"], a["dt"], a["ks"],
+            a["vs"]]
+    types = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, f32, i32, i32, i32, f32, f32]
+    f = getattr(L, name)
+    if name == "pd_decode_static_ws":
+        f.argtypes = types + [P]
+        return f(*head, None)
+    f.argtypes = types + [P, ctypes.c_size_t, P]
+    return f(*head, 0x6000, 1 << 20, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=96), 2),                  # head_dim not built: refused before choosing S
+    (dict(D=96, B=70000), 1),         # too many sequences comes first
+    (dict(Hq=34, Hkv=2), 2),          # group of 17
+    (dict(Hq=6, Hkv=4), 1),           # GQA ratio not integral
+    (dict(dt=7), 2),                  # unknown cache form
+    (dict(S=5000), 1),                # split count out of range
+    (dict(dt=1, ks=0.0), 1),          # FP8 needs a positive scale
+    (dict(out=0x7004), 1),            # misaligned output
+    (dict(scale=float("inf")), 1),
+])
+def test_static_workspace_answers_like_pd_decode(pdlib, kw, code):
+    """pd_decode_static_ws runs pd_decode's own checks in pd_decode's order,
+    before any CUDA call, so a malformed request gets the same status from
+    both (here on a host without a GPU)."""
+    _, L = pdlib
+    assert _decode_entry(L, "pd_decode", **kw) == code
+    assert _decode_entry(L, "pd_decode_static_ws", **kw) == code
+    assert _decode_entry(L, "pd_decode_crosscheck", **kw) == code
+
+
+def test_fp8_scale_matches_oracle(pdlib):
+    """pd_fp8_scale (host) against oracle_fp8_scale, bit for bit: special
+    values and 200k random absmax values over the whole float range."""
+    import numpy as np
+    import oracle
+    from paged_kv_split_gb300 import inputs
+    _, L = pdlib
+    L.pd_fp8_scale.argtypes, L.pd_fp8_scale.restype = [ctypes.c_float], ctypes.c_float
+    orc = oracle.get()
+    special = [0.0, -0.0, float("nan"), float("inf"), 1e-45, 1.1754942e-38, 448.0, 1.0, 3.0e38,
+               -5.0, 6.0, 2.0 ** -9]
+    rnd = inputs.uniform_int(71, 200000, 0, 0x7F7FFFFF).astype(np.uint32).view(np.float32)
+    for x in special + [float(v) for v in rnd]:
+        got = np.float32(L.pd_fp8_scale(x))
+        want = np.float32(orc.fp8_scale(x))
+        assert got.view(np.uint32) == want.view(np.uint32), (x, got, want)

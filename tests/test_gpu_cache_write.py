@@ -90,6 +90,23 @@ def test_fp8_calibrate_matches_oracle(orc):
     assert (ks, vs) == U.fp8_scales(orc, case)
 
 
+def test_fp8_scales_from_absmax_match_oracle(orc):
+    """The device scale kernel against oracle_fp8_scale, bit for bit, on
+    special values (0, NaN, denormals, the largest finite) and random ones."""
+    from paged_kv_split_gb300 import binding
+    special = np.array([0.0, -0.0, np.nan, 1e-45, 1.17e-38, 448.0, 1.0, 3.4e38, np.inf, -2.0],
+                       np.float32)
+    rnd = (inputs.normal_bf16(63, (5000,), std=40.0).astype(np.uint32) << 16).view(np.float32)
+    bits = inputs.uniform_int(64, 5000, 0, 0x7F7FFFFF).astype(np.uint32).view(np.float32)
+    amax = np.concatenate([special, np.abs(rnd), bits]).astype(np.float32)
+    a = torch.from_numpy(amax).cuda()
+    out = torch.empty_like(a)
+    binding.pd_fp8_scales_from_absmax(a, out)
+    got = out.cpu().numpy()
+    want = np.array([orc.fp8_scale(float(x)) for x in amax], np.float32)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
 def test_slots_out_of_pool_are_skipped_and_flagged(orc):
     from paged_kv_split_gb300 import binding
     case = inputs.make_case("bad", [20], 4, 2, 64, 16, seed=62, extra_blocks=1)

@@ -7,7 +7,9 @@ row sees (the oracle pins make that bit-identical to oracle_prefill).
 Edge cases: empty sequences, a fresh prompt (q_len == L), one query per
 sequence, group sizes that do not divide the CTA's rows, a q_len above
 max_q_len, pages outside the pool, strided rows and graph replay. Every test
-runs on both kernels (tcgen05 and mma.sync)."""
+runs on both kernels (tcgen05 through pd_prefill, mma.sync through
+pd_prefill_crosscheck)."""
+import functools
 import zlib
 from concurrent.futures import ThreadPoolExecutor
 
@@ -23,12 +25,14 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(params=["tcgen05", "mma_sync"], autouse=True)
 def prefill_kernel(request, monkeypatch):
-    """Every test runs on both prefill kernels: the tcgen05 one (default) and
-    the mma.sync one (PD_PREFILL_KERNEL=mma, read by libpd.so on each call)."""
+    """Every test runs on both prefill kernels: pd_prefill (tcgen05) and
+    pd_prefill_crosscheck (mma.sync), chosen through the binding's
+    `crosscheck` argument."""
     if request.param == "mma_sync":
-        monkeypatch.setenv("PD_PREFILL_KERNEL", "mma")
-    else:
-        monkeypatch.delenv("PD_PREFILL_KERNEL", raising=False)
+        from paged_kv_split_gb300 import binding as B
+        monkeypatch.setattr(B, "pd_prefill", functools.partial(B.pd_prefill, crosscheck=True))
+        monkeypatch.setattr(B, "pd_prefill_strided",
+                            functools.partial(B.pd_prefill_strided, crosscheck=True))
     return request.param
 
 CASES = [
@@ -201,32 +205,50 @@ def test_unsupported_forms_are_refused():
                          num_blocks=case.num_blocks, scale=case.scale, **kw)
 
 
-# ---- the chunked-prefill workload at full size (sampled rows) --------------
-def test_chunked_prefill_workload_sampled_rows(orc):
+# ---- the chunked-prefill workload at full size, every row ------------------
+_FULL_REF = {}
+
+
+def _oracle_prefill_row_blocks(orc, case, kh, vh, parts=4, threads=16):
+    """Causal oracle_prefill over every query row, each sequence cut into
+    `parts` blocks of rows so that all host cores work. Rows [i0, i1) of a
+    sequence with L keys and q_len queries are presented as their own
+    sequence of i1 - i0 queries over its first L - q_len + i1 keys: query j
+    then sits at position L - q_len + i0 + j and sees exactly the keys that
+    row i0 + j sees in the whole sequence."""
+    cu = case.extra["cu_q"]
+    tasks = []
+    for b in range(case.num_seqs):
+        ql, L = int(cu[b + 1] - cu[b]), int(case.seq_lens[b])
+        edges = np.linspace(0, ql, parts + 1).astype(int)
+        tasks += [(b, int(i0), int(i1), L, ql) for i0, i1 in zip(edges[:-1], edges[1:]) if i1 > i0]
+
+    def run(t):
+        b, i0, i1, L, ql = t
+        r0 = int(cu[b])
+        return orc.prefill(case.q[r0 + i0:r0 + i1], np.array([0, i1 - i0], np.int32), kh, vh,
+                           case.block_tables[b:b + 1], np.array([L - ql + i1], np.int32),
+                           case.num_kv_heads, case.block_size, case.num_blocks, case.scale,
+                           True, case.sliding_window)[0]
+
+    with ThreadPoolExecutor(threads) as ex:
+        parts_out = list(ex.map(run, tasks))
+    return np.concatenate(parts_out)
+
+
+def test_chunked_prefill_workload_every_row(orc):
+    """The bench's chunked-prefill workload (8 sequences, 512-token chunks after
+    up to 3584 cached tokens, 32 q / 8 kv heads, D=128): every element of all
+    4096 query rows against oracle_prefill, on both kernels (the oracle's
+    result is computed once per process and reused)."""
     case = inputs.prefill_chunked()
     kc, vc = U.gpu_write_cache(case, 0)
     got = gpu_prefill(case, kc, vc)
     assert np.all(np.isfinite(U.bf16_bits_to_f32(got)))
-    kh, vh = kc.cpu().numpy(), vc.cpu().numpy()
-    cu = case.extra["cu_q"]
-    rng = np.random.default_rng(7)
-    picks = []
-    for b in range(case.num_seqs):
-        ql = int(cu[b + 1] - cu[b])
-        # the first and last row of the chunk, tile edges and random rows
-        rows = {0, ql - 1, 15, 16, ql // 2} | set(rng.integers(0, ql, 4).tolist())
-        picks += [(b, i) for i in sorted(r for r in rows if 0 <= r < ql)]
-
-    def one(bi):
-        b, i = bi
-        L, ql = int(case.seq_lens[b]), int(cu[b + 1] - cu[b])
-        p = L - ql + i
-        o, _ = orc.decode(case.q[cu[b] + i][None], kh, vh, case.block_tables[b:b + 1],
-                          np.array([p + 1], np.int32), case.num_kv_heads, case.block_size,
-                          case.num_blocks, case.scale)
-        return o[0]
-
-    with ThreadPoolExecutor(16) as ex:
-        ref = np.stack(list(ex.map(one, picks)))
-    rows = np.array([cu[b] + i for b, i in picks])
-    U.assert_close(got[rows], ref, what=f"prefill {case.name} ({len(picks)} sampled rows)")
+    if case.name not in _FULL_REF:
+        _FULL_REF[case.name] = _oracle_prefill_row_blocks(orc, case, kc.cpu().numpy(),
+                                                          vc.cpu().numpy())
+    ref = _FULL_REF[case.name]
+    assert got.shape == ref.shape == (int(case.extra["cu_q"][-1]), case.num_q_heads,
+                                      case.head_dim)
+    U.assert_close(got, ref, what=f"prefill {case.name} (all {got.shape[0]} rows)")

@@ -21,6 +21,14 @@ def _sdpa_all(orc):
             TD.test_oracle_matches_sdpa_f64(orc, kv, i)
 
 
+def _e4m3_out_all(orc):
+    from tests import test_oracle_e4m3_out as TE
+    for kv in (0, 1, 2):
+        for sc in (0.0078125, 0.013, 3.0):
+            TE.test_length_one_is_the_encoded_value(orc, kv, sc)
+        TE.test_codes_encode_the_fp32_output(orc, kv)
+
+
 def _prefill_all(orc):
     from tests import test_oracle_prefill as TP
     for idx in range(len(TP.PREFILL_CASES)):
@@ -70,6 +78,12 @@ MUTANTS = [
      "const int64_t qrow = static_cast<int64_t>(cu_q[b]) + i / 2;", [_prefill_all]),
     ("fp8 quantise multiplies", "return std::isnan(x) ? x : x / s;",
      "return std::isnan(x) ? x : x * s;", [TC.test_fp8_cache_matches_torch_e4m3]),
+    ("e4m3 output scale multiplies", "out_codes[i] = e4m3_code(quotient(o[i], out_scale));",
+     "out_codes[i] = e4m3_code(o[i] * out_scale);", [_e4m3_out_all]),
+    ("e4m3 output encodes the bf16-rounded value",
+     "out_codes[i] = e4m3_code(quotient(o[i], out_scale));",
+     "out_codes[i] = e4m3_code(quotient(bf16_value(out_bf16[i]), out_scale));",
+     [_e4m3_out_all]),
 ]
 
 
