@@ -414,11 +414,14 @@ int pd_decode_static_ws(const void* q, const void* k_cache, const void* v_cache,
  *               keys j <= its position; 0: every query sees all L_b keys.
  *   sliding_window  W > 0 keeps keys j with position - j < W; 0 = off.
  * Scores, softmax and the bf16 output follow pd_decode (scale after the dot
- * product, 1e-20 guard). Cache, block tables, scale, status codes and device
- * flags as in pd_decode. Supported: kv_dtype PD_KV_BF16, head_dim 64 or 128,
- * block_size 16 or 32, G = num_q_heads / num_kv_heads <= 16; anything else
- * returns PD_ERR_UNSUPPORTED. No workspace: each query tile writes its rows.
- * The work runs on the tcgen05 tensor cores (accumulators in TMEM).
+ * product, 1e-20 guard). Cache (all three forms, with k_scale / v_scale for
+ * FP8), block tables, scale, status codes and device flags as in pd_decode
+ * ([AstrAI]: prefill kernels templated on the paged KV source). Supported:
+ * head_dim 64, 128 or 256, block_size 16 or 32, G = num_q_heads /
+ * num_kv_heads <= 16; anything else returns PD_ERR_UNSUPPORTED. No
+ * workspace: each query tile writes its rows. BF16 caches run on the tcgen05
+ * tensor cores (accumulators in TMEM); FP8 and NVFP4 caches on mma.sync
+ * tiles, each stage widened once to f16 (exact) before its MMAs.
  * Device pointers owned by the caller, 16-byte aligned; enqueued on `stream`,
  * never synchronises. */
 int pd_prefill(const void* q, int64_t q_stride, const int32_t* cu_q, const void* k_cache,
@@ -446,7 +449,8 @@ int pd_decode_crosscheck(const void* q, const void* k_cache, const void* v_cache
                          void* workspace, size_t workspace_bytes, void* stream);
 
 /* pd_prefill on mma.sync tensor-core tiles (64 query rows per CTA) instead of
- * the tcgen05 kernel. Same arguments and support as pd_prefill. */
+ * the tcgen05 kernel. Same arguments and support as pd_prefill (for FP8 and
+ * NVFP4 caches pd_prefill runs this kernel itself). */
 int pd_prefill_crosscheck(const void* q, int64_t q_stride, const int32_t* cu_q,
                           const void* k_cache, const void* v_cache, const int32_t* block_tables,
                           const int32_t* seq_lens, void* out, int64_t out_stride,

@@ -91,7 +91,7 @@ struct Cfg {
   static constexpr int kCacheStageBytes = (kDataBytes + kScaleBytes + 1023) / 1024 * 1024;
   static constexpr int kStageBytes = 2 * kCacheStageBytes;
   static constexpr int kStagesRaw =
-      (kDSplit == 1 ? PD_MMA_RING_BYTES_SMALL_D : PD_MMA_RING_BYTES_LARGE_D) / kStageBytes;
+      (kDSplit == 1 ? ring_bytes_small_d<FMT>() : PD_MMA_RING_BYTES_LARGE_D) / kStageBytes;
   static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
   static constexpr int kRingBytes = kStages * kStageBytes;
   // cross-warp score sums (head_dim split): 2 buffers x 4 warps x m-tiles x 32 lanes x 4*NT
@@ -99,10 +99,15 @@ struct Cfg {
   static constexpr int kQMaxBytes = kDSplit == 4 ? NT * 4 * 8 * 4 : 0;  // [NT][warp][8] floats
   static constexpr int kHW = 8 * NT;                        // q-head columns of the tiles
   static constexpr int kMStride = D + 4;                    // floats per merge-slice row
-  // end-of-item merge (head_dim <= 128): a [kHW][D+4] slice, per-warp m and l
-  // (two buffers, by item parity), and the merged m and l of each column
+  // the four warps' unscaled O of a piece fit the piece's held last stage (as
+  // [warp][head][D] floats) for every group this instantiation serves: then
+  // the merge needs no slice of its own
+  static constexpr bool kMergeInStage = 4 * kHW * D * 4 <= kStageBytes;
+  // end-of-item merge (head_dim <= 128): a [kHW][D+4] slice (unless the held
+  // stage takes the merge), per-warp m and l (two buffers, by item parity),
+  // and the merged m and l of each column
   static constexpr int kMergeBytes =
-      kDSplit == 1 ? (kHW * kMStride + 2 * 2 * 4 * kHW + 2 * kHW) * 4 : 0;
+      kDSplit == 1 ? ((kMergeInStage ? 0 : kHW * kMStride) + 2 * 2 * 4 * kHW + 2 * kHW) * 4 : 0;
   static constexpr int kQSlots = kDSplit == 1 ? 2 : 1;      // q of the next item lands early
   static constexpr int kMergeOffset = kRingBytes + kRedBytes + kQMaxBytes;
   static constexpr int kMetaOffset = (kMergeOffset + kMergeBytes + 15) / 16 * 16;
@@ -126,18 +131,6 @@ struct Cfg {
 
 // Consumer-warp barrier on an mbarrier (one arrival per warp, bounded wait),
 // so that a stalled peer ends in an error instead of a hang.
-// Named barrier 1 over the four consumer warps that also ANDs a predicate
-// across them: every consumer thread gets the same answer.
-__device__ __forceinline__ bool consumers_vote(bool ok) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(ok)), "n"(kConsumerWarps * 32)
-      : "memory");
-  return r != 0;
-}
 __device__ __forceinline__ void consumers_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
@@ -157,7 +150,8 @@ struct ConsumerSync {
 };
 
 template <int FMT, int D, int NT, int BS>
-__global__ void __launch_bounds__(kMmaThreads)
+__global__ void __launch_bounds__(kMmaThreads,
+                                  partial_min_blocks(Cfg<FMT, D, NT, BS>::smem_bytes(8 * NT), NT))
     partial_balanced_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_ks,
@@ -182,8 +176,8 @@ __global__ void __launch_bounds__(kMmaThreads)
   unsigned char* ring = smem;
   float* red = reinterpret_cast<float*>(smem + C::kRingBytes);
   float* qmax_s = reinterpret_cast<float*>(smem + C::kRingBytes + C::kRedBytes);
-  float* mslice = reinterpret_cast<float*>(smem + C::kMergeOffset);  // [kHW][D+4]
-  float* mrec = mslice + C::kHW * C::kMStride;                        // [2][4][kHW]
+  float* mslice = reinterpret_cast<float*>(smem + C::kMergeOffset);  // [kHW][D+4], if any
+  float* mrec = mslice + (C::kMergeInStage ? 0 : C::kHW * C::kMStride);  // [2][4][kHW]
   float* lrec = mrec + 2 * 4 * C::kHW;                                // [2][4][kHW]
   float* fin_m = lrec + 2 * 4 * C::kHW;                               // [kHW]
   float* fin_l = fin_m + C::kHW;                                      // [kHW]
@@ -536,8 +530,9 @@ __global__ void __launch_bounds__(kMmaThreads)
             lr[warp * C::kHW + hc] = l_run[nt][j];
           }
         }
-      const int ostride = D + 4;  // padded rows: conflict-free fragment stores
-      if (4 * G * ostride * 4 <= C::kStageBytes) {
+      // padded rows (conflict-free fragment stores) where they fit the stage
+      const int ostride = 4 * G * (D + 4) * 4 <= C::kStageBytes ? D + 4 : D;
+      if (C::kMergeInStage || 4 * G * ostride * 4 <= C::kStageBytes) {
         // the four warps' unscaled O in the held stage [warp][head][D+4] (once
         // every warp is done reading its keys), then every thread merges whole
         // output elements (warps 0..3 in order)

@@ -84,7 +84,7 @@ struct Cfg {
   static constexpr int kCacheStageBytes = (kDataBytes + kScaleBytes + 1023) / 1024 * 1024;
   static constexpr int kStageBytes = 2 * kCacheStageBytes;
   static constexpr int kStagesRaw =
-      (kDSplit == 1 ? PD_MMA_RING_BYTES_SMALL_D : PD_MMA_RING_BYTES_LARGE_D) / kStageBytes;
+      (kDSplit == 1 ? ring_bytes_small_d<FMT>() : PD_MMA_RING_BYTES_LARGE_D) / kStageBytes;
   static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
   static constexpr int kRingBytes = kStages * kStageBytes;
   // cross-warp score sums (head_dim split): 2 buffers x 4 warps x m-tiles x 32 lanes x 4*NT
@@ -106,7 +106,8 @@ struct Cfg {
 };
 
 template <int FMT, int D, int NT, int BS>
-__global__ void __launch_bounds__(kMmaThreads)
+__global__ void __launch_bounds__(kMmaThreads,
+                                  partial_min_blocks(Cfg<FMT, D, NT, BS>::kSmemBytes, NT))
     partial_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_ks,

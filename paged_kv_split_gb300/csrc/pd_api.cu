@@ -270,9 +270,20 @@ size_t balanced_ws_bytes(int64_t num_pieces, int G, int D) {
   return o + ml;
 }
 
+// Cost of a piece boundary inside a share, in keys: a piece ends in a partly
+// filled 64-key tile (half a tile on average) and adds a merge and a q load.
+// Measured: a CTA's time grows by about 1 us per extra piece, which is what
+// 2 to 3 pages of 16 rows take at every cache form's rate.
+constexpr int kPieceCostKeys = 40;
+
 // Cut the line of (sequence, kv head) key-page ranges, laid end to end in
-// sequence-major order, into num_ctas equal shares (page granularity); every
-// share that crosses a range boundary becomes several pieces.
+// sequence-major order, into num_ctas shares of equal cost (page
+// granularity); every share that crosses a range boundary becomes several
+// pieces. The cost of a share is its pages plus kPieceCostKeys for each range
+// boundary inside it: the cut runs on a virtual line (1/16 page units) with a
+// gap of that cost after every range, so a share that takes in a boundary
+// gets correspondingly fewer pages. (The gap is dropped when shares are only
+// a few pages long, so that no share falls into a gap.)
 int build_balanced_plan(const int32_t* lens, int B, int Hq, int Hkv, int D, int bs, int mbs,
                         int W, int kv_dtype, int num_sms, int32_t* plan, size_t plan_bytes,
                         int32_t* out_ctas, int32_t* out_pieces, size_t* out_ws) {
@@ -289,13 +300,20 @@ int build_balanced_plan(const int32_t* lens, int B, int Hq, int Hkv, int D, int 
   if (NC > kMaxBalancedCtas) NC = kMaxBalancedCtas;
   if (NC > T) NC = T;
   const int64_t segs = static_cast<int64_t>(B) * Hkv;
+  // the virtual line: 16 units per page, a gap after every non-empty range
+  constexpr int64_t kU = 16;
+  int64_t ranges = 0;
+  for (int b = 0; b < B; ++b) ranges += P[b] > 0 ? Hkv : 0;
+  int64_t gap = (kPieceCostKeys * kU + bs / 2) / bs;
+  if (NC == 0 || T * kU < 4 * gap * NC) gap = 0;
+  const int64_t VT = T * kU + gap * (ranges > 0 ? ranges - 1 : 0);
   // pieces: one per range, plus one per share boundary strictly inside a range
   std::vector<int32_t> pieces;
   std::vector<int32_t> cta_begin(NC + 1, 0);
   std::vector<int32_t> seg(2 * segs, 0);
   pieces.reserve(4 * (segs + NC));
-  auto bound = [&](int64_t c) { return NC > 0 ? c * T / NC : 0; };  // share c starts here
-  int64_t pos = 0;  // line position of the current range's first page
+  auto bound = [&](int64_t c) { return NC > 0 ? c * VT / NC : 0; };  // share c starts here
+  int64_t pos = 0;  // virtual position of the current range's first page
   int64_t c = 0;    // share holding `pos`
   int64_t np = 0;
   for (int b = 0; b < B; ++b) {
@@ -307,11 +325,13 @@ int build_balanced_plan(const int32_t* lens, int B, int Hq, int Hkv, int D, int 
       if (P[b] == 0) continue;
       int64_t a = 0;  // pages of this range already cut
       while (a < P[b]) {
-        while (c + 1 < NC && bound(c + 1) <= pos + a) {
+        while (c + 1 < NC && bound(c + 1) <= pos + a * kU) {
           ++c;
           cta_begin[c] = static_cast<int32_t>(np);
         }
-        const int64_t e = std::min<int64_t>(P[b], (c + 1 < NC ? bound(c + 1) : T) - pos);
+        // the pages whose virtual start lies before the next share's start
+        const int64_t next = c + 1 < NC ? bound(c + 1) : VT;
+        const int64_t e = std::min<int64_t>(P[b], (next - pos + kU - 1) / kU);
         const int t_begin = std::max(lo, static_cast<int>((page0 + a) * bs));
         const int t_end = std::min(L[b], static_cast<int>((page0 + e) * bs));
         pieces.push_back(static_cast<int32_t>(sid));
@@ -324,7 +344,7 @@ int build_balanced_plan(const int32_t* lens, int B, int Hq, int Hkv, int D, int 
       const int32_t count = static_cast<int32_t>(np) - seg[2 * sid];
       seg[2 * sid + 1] = count;
       if (count == 1) pieces[4 * (np - 1) + 3] = 1;  // its head's only piece: write out
-      pos += P[b];
+      pos += P[b] * kU + gap;
     }
   }
   for (int64_t k = c + 1; k <= NC; ++k) cta_begin[k] = static_cast<int32_t>(np);
@@ -857,8 +877,6 @@ int prefill_impl(const void* q, int64_t q_stride, const int32_t* cu_q, const voi
                  int32_t max_blocks_per_seq, int64_t num_blocks, float scale, int32_t causal,
                  int32_t sliding_window, int32_t kv_dtype, float k_scale, float v_scale,
                  void* stream, bool mma_sync) {
-  (void)k_scale;
-  (void)v_scale;
   if (num_seqs < 0 || num_seqs > 65535 || max_q_len < 0) return PD_ERR_INVALID_ARG;
   if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
     return PD_ERR_INVALID_ARG;
@@ -866,7 +884,9 @@ int prefill_impl(const void* q, int64_t q_stride, const int32_t* cu_q, const voi
   if (G > kMaxGroup || num_kv_heads > 65535) return PD_ERR_UNSUPPORTED;
   if (!dtype_ok(kv_dtype) || !head_dim_ok(head_dim) || !block_size_ok(block_size))
     return PD_ERR_UNSUPPORTED;
-  if (kv_dtype != PD_KV_BF16 || head_dim > 128) return PD_ERR_UNSUPPORTED;
+  if (head_dim > 256) return PD_ERR_UNSUPPORTED;
+  if (kv_dtype == PD_KV_FP8_E4M3 && !(scale_ok(k_scale) && scale_ok(v_scale)))
+    return PD_ERR_INVALID_ARG;
   if (max_blocks_per_seq <= 0 || num_blocks <= 0 || sliding_window < 0) return PD_ERR_INVALID_ARG;
   if (static_cast<int64_t>(max_blocks_per_seq) * block_size > (int64_t{1} << 30))
     return PD_ERR_INVALID_ARG;
@@ -899,10 +919,16 @@ int prefill_impl(const void* q, int64_t q_stride, const int32_t* cu_q, const voi
   a.causal = causal != 0;
   a.sliding_window = sliding_window;
   a.scale_log2 = scale * kLog2e;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (mma_sync) {
+  // the tcgen05 kernel reads BF16 caches; FP8 / NVFP4 caches (and the
+  // cross-check) run on the mma.sync kernel, which widens each stage to f16
+  if (mma_sync || kv_dtype != PD_KV_BF16) {
     a.tokens_per_cta = 64 / G;
-    return cuda_status(launch_prefill(a, k_cache, v_cache, head_dim, max_q_len, st));
+    return cuda_status(launch_prefill(a, k_cache, v_cache, head_dim, kv_dtype, max_q_len, st));
   }
   a.tokens_per_cta = 128 / G;
   return cuda_status(launch_prefill_umma(a, k_cache, v_cache, head_dim, max_q_len, st));

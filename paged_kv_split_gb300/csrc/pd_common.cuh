@@ -202,6 +202,9 @@ struct PrefillArgs {
   int tokens_per_cta;            // query tokens of one CTA: 64 / group
   int causal, sliding_window;
   float scale_log2;              // scale * log2(e)
+  const void* k_cache;           // the caches (read by bulk copies for NVFP4)
+  const void* v_cache;
+  float k_scale, v_scale;        // FP8 per-tensor scales
 };
 
 // Sequence length as the kernels use it: clamped to the block table, with a
@@ -254,11 +257,12 @@ cudaError_t launch_decode_partial_balanced(const DecodeArgs& a, int head_dim, in
 // Resident CTAs per SM of the balanced partial kernel for a GQA group size.
 int balanced_ctas_per_sm(int kv_dtype, int head_dim, int group);
 cudaError_t launch_decode_combine(const CombineArgs& a, int head_dim, cudaStream_t st);
-// Paged prefill over a BF16 cache (head_dim 64 / 128); grid.x = q tiles.
-// launch_prefill: mma.sync kernel, 64 rows per CTA (tokens_per_cta = 64 / G);
-// launch_prefill_umma: tcgen05 kernel, 128 rows per CTA (128 / G).
+// Paged prefill (head_dim 64 / 128 / 256); grid.x = q tiles.
+// launch_prefill: mma.sync kernel, any cache form, 64 rows per CTA
+// (tokens_per_cta = 64 / G); launch_prefill_umma: tcgen05 kernel, BF16
+// caches, 128 rows per CTA (128 / G).
 cudaError_t launch_prefill(const PrefillArgs& a, const void* k_cache, const void* v_cache,
-                           int head_dim, int max_q_len, cudaStream_t st);
+                           int head_dim, int kv_dtype, int max_q_len, cudaStream_t st);
 cudaError_t launch_prefill_umma(const PrefillArgs& a, const void* k_cache, const void* v_cache,
                                 int head_dim, int max_q_len, cudaStream_t st);
 }  // namespace pd

@@ -51,6 +51,10 @@ using namespace ::pd::mma;
 #ifndef PD_UMMA_PREFILL_STAGES
 #define PD_UMMA_PREFILL_STAGES 0  // 0: five stages at head_dim 128, four at 64
 #endif
+// CTAs per SM the kernel is compiled for (its register cap)
+#ifndef PD_UMMA_PREFILL_MIN_BLOCKS
+#define PD_UMMA_PREFILL_MIN_BLOCKS 1
+#endif
 // The running max that P is taken against moves only when a row's tile max
 // exceeds it by more than this (log2 units): P <= 2^8 in bf16, and O and l
 // are rescaled in TMEM a few times per row instead of nearly every tile.
@@ -63,7 +67,10 @@ constexpr int kProdWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kUmmaThreads = 10 * 32;
 constexpr int kRowsU = 128;           // (token, q head) rows per CTA = UMMA M
-constexpr int kTmemCols = 256;        // S0 [0, 64), S1 [64, 128), O [128, 128 + D)
+// TMEM columns: S0 [0, 64), S1 [64, 128), O [128, 128 + D), rounded up to a
+// power of two (head_dim 256 takes all 512 columns of the SM)
+template <int D>
+constexpr int tmem_cols() { return D <= 128 ? 256 : 512; }
 
 template <int D, int BS>
 struct UCfg {
@@ -75,8 +82,11 @@ struct UCfg {
   static constexpr int kPBytes = kRowsU * 128;         // P tile: 128 rows x 64 keys bf16
   static constexpr int kCacheStageBytes = kKT * 2 * D;
   static constexpr int kStageBytes = 2 * kCacheStageBytes;
+  // five stages at head_dim 128, four at 64; at 256 a stage is 64 KB and two
+  // fit beside the 64 KB Q tile
   static constexpr int kStages =
-      PD_UMMA_PREFILL_STAGES > 0 ? PD_UMMA_PREFILL_STAGES : (D == 128 ? 5 : 4);
+      PD_UMMA_PREFILL_STAGES > 0 ? PD_UMMA_PREFILL_STAGES
+                                 : (D == 128 ? 5 : (D == 64 ? 4 : 2));
   static constexpr int kQOff = 0;
   static constexpr int kPOff = kQOff + kQBytes;
   static constexpr int kRingOff = kPOff + kPBytes;
@@ -95,6 +105,7 @@ struct UCfg {
   static constexpr uint32_t kCopyBytes = kBR * 2 * D;
   static constexpr int kKS = D / 16;  // K steps of S
   static_assert(kCacheStageBytes % 1024 == 0 && kQBytes % 1024 == 0, "1024-byte aligned tiles");
+  static_assert(kSmemBytes <= 227 * 1024, "one CTA's shared memory");
 };
 
 // tcgen05 shared-memory matrix descriptor: start address, leading and stride
@@ -164,7 +175,7 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 }
 
 template <int D, int BS>
-__global__ void __launch_bounds__(kUmmaThreads, 1)
+__global__ void __launch_bounds__(kUmmaThreads, PD_UMMA_PREFILL_MIN_BLOCKS)
     prefill_umma_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
   using C = UCfg<D, BS>;
@@ -270,7 +281,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(holder)),
-                 "n"(kTmemCols)
+                 "n"(tmem_cols<D>())
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -577,7 +588,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
   if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "n"(kTmemCols)
+                 "n"(tmem_cols<D>())
                  : "memory");
   }
 }
@@ -631,6 +642,9 @@ cudaError_t launch_prefill_umma(const PrefillArgs& a, const void* k_cache, const
     case 128:
       return bs16 ? launch_umma_cfg<128, 16>(a, k_cache, v_cache, max_q_len, st)
                   : launch_umma_cfg<128, 32>(a, k_cache, v_cache, max_q_len, st);
+    case 256:
+      return bs16 ? launch_umma_cfg<256, 16>(a, k_cache, v_cache, max_q_len, st)
+                  : launch_umma_cfg<256, 32>(a, k_cache, v_cache, max_q_len, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -180,7 +180,7 @@ def test_prefill_validation(pdlib):
     assert call(mq=0) == 0
     assert call(dt=1) == 2                # FP8 / NVFP4 caches: not built for prefill
     assert call(dt=2) == 2
-    assert call(D=256) == 2               # head_dim above 128: not built for prefill
+    assert call(D=512) == 2               # head_dim 512: not built for prefill
     assert call(D=96) == 2
     assert call(bs=8) == 2
     assert call(Hq=34, Hkv=2) == 2        # group of 17 > 16

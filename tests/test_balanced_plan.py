@@ -1,6 +1,8 @@
 """The balanced plan (pd_balanced_plan, host only): it must cover every
 (sequence, kv head) key range exactly once, in order, give every CTA the same
-number of pages to within one, and describe itself consistently. CPU only."""
+cost (its pages plus 40 keys' worth for each extra piece) to within the
+page rounding at its two ends and a piece's cost at each, and describe itself
+consistently. CPU only."""
 import numpy as np
 import pytest
 
@@ -79,11 +81,15 @@ def test_plan_covers_every_range_once_and_balances(name, lens, kw):
             assert (ps[:, 1][1:] % bs == 0).all()  # cuts fall on page boundaries
             assert ((ps[:, 3] & 1) == (1 if count == 1 else 0)).all()
     assert seg[:, 1].sum() == npc
-    # balance: pages per CTA within one of each other
-    per_cta = [sum(_pages(int(p[1]), int(p[2]), bs) for p in pieces[cta[c]:cta[c + 1]])
-               for c in range(nc)]
-    assert sum(per_cta) == total_pages
-    assert max(per_cta) - min(per_cta) <= 1
+    # balance: the cost of a CTA's share (pages, plus 40 / bs pages for every
+    # piece after its first) is the same for every CTA up to the rounding at
+    # the share's two ends (a page, and a piece's cost at each end)
+    per_cta = np.array([sum(_pages(int(p[1]), int(p[2]), bs)
+                            for p in pieces[cta[c]:cta[c + 1]]) for c in range(nc)])
+    assert per_cta.sum() == total_pages
+    kappa = 40 / bs
+    cost = per_cta + kappa * (np.diff(cta) - 1)
+    assert cost.max() - cost.min() <= 2 + 2 * kappa
     assert plan.workspace_bytes >= npc * G * (D + 2) * 4
 
 

@@ -46,6 +46,8 @@ CASES = [
     ("g16", [150, 60], [33, 60], 16, 1, 64, 32, 0),
     ("g8_window_ragged", [500, 211, 64], [130, 211, 1], 32, 4, 128, 16, 100),
     ("empty_and_zero_q", [0, 90, 40], [0, 0, 40], 8, 2, 64, 16, 0),
+    ("d256", [300, 77], [130, 77], 8, 2, 256, 16, 0),
+    ("d256_g8_window_bs32", [400, 129], [200, 64], 16, 2, 256, 32, 100),
 ]
 
 
@@ -56,7 +58,8 @@ def _case(spec, seed_base=500):
                                     sliding_window=w, extra_blocks=2)
 
 
-def gpu_prefill(case, kc, vc, causal=True, max_q_len=None, block_tables=None):
+def gpu_prefill(case, kc, vc, causal=True, max_q_len=None, block_tables=None, kv_dtype=0,
+                k_scale=1.0, v_scale=1.0):
     from paged_kv_split_gb300 import binding as B
     cu = case.extra["cu_q"]
     q = U.bf16_dev(case.q)
@@ -66,12 +69,14 @@ def gpu_prefill(case, kc, vc, causal=True, max_q_len=None, block_tables=None):
     B.pd_prefill(q, U.to_dev(cu), kc, vc, U.to_dev(bt), U.to_dev(case.seq_lens), out,
                  max_q_len=mq, num_kv_heads=case.num_kv_heads, block_size=case.block_size,
                  num_blocks=case.num_blocks, scale=case.scale, causal=causal,
-                 sliding_window=case.sliding_window)
+                 sliding_window=case.sliding_window, kv_dtype=kv_dtype, k_scale=k_scale,
+                 v_scale=v_scale)
     torch.cuda.synchronize()
     return out.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def oracle_prefill(orc, case, kc_host, vc_host, causal=True, threads=16):
+def oracle_prefill(orc, case, kc_host, vc_host, causal=True, threads=16, kv_dtype=0,
+                   k_scale=1.0, v_scale=1.0):
     """oracle_prefill, one call per sequence on a thread pool (the ctypes call
     releases the GIL; each call is the plain single-threaded oracle)."""
     cu = case.extra["cu_q"]
@@ -81,21 +86,30 @@ def oracle_prefill(orc, case, kc_host, vc_host, causal=True, threads=16):
         sub_cu = np.array([0, r1 - r0], np.int32)
         return orc.prefill(case.q[r0:r1], sub_cu, kc_host, vc_host, case.block_tables[b:b + 1],
                            case.seq_lens[b:b + 1], case.num_kv_heads, case.block_size,
-                           case.num_blocks, case.scale, causal, case.sliding_window)[0]
+                           case.num_blocks, case.scale, causal, case.sliding_window, kv_dtype,
+                           k_scale, v_scale)[0]
 
     with ThreadPoolExecutor(threads) as ex:
         parts = list(ex.map(run, range(case.num_seqs)))
     return np.concatenate(parts) if parts else np.zeros(case.q.shape, np.uint16)
 
 
+@pytest.mark.parametrize("kv_dtype", [0, 1, 2], ids=["bf16", "fp8", "nvfp4"])
 @pytest.mark.parametrize("causal", [True, False], ids=["causal", "full"])
 @pytest.mark.parametrize("spec", CASES, ids=[c[0] for c in CASES])
-def test_small_parity(orc, spec, causal):
+def test_small_parity(orc, spec, causal, kv_dtype):
+    """Every element against oracle_prefill, the quantised caches read from the
+    same GPU-written bytes (checked bit-exact against the oracle's first)."""
     case = _case(spec)
-    kc, vc = U.gpu_write_cache(case, 0)
-    got = gpu_prefill(case, kc, vc, causal)
-    ref = oracle_prefill(orc, case, kc.cpu().numpy(), vc.cpu().numpy(), causal)
-    U.assert_close(got, ref, what=f"prefill {case.name} causal={causal}")
+    ks, vs = U.fp8_scales(orc, case) if kv_dtype == 1 else (1.0, 1.0)
+    kc, vc = U.gpu_write_cache(case, kv_dtype, ks, vs)
+    kh, vh = kc.cpu().numpy(), vc.cpu().numpy()
+    if kv_dtype:
+        okc, ovc = U.oracle_write_cache(orc, case, kv_dtype, ks, vs)
+        assert np.array_equal(kh, okc) and np.array_equal(vh, ovc), "cache bytes differ"
+    got = gpu_prefill(case, kc, vc, causal, kv_dtype=kv_dtype, k_scale=ks, v_scale=vs)
+    ref = oracle_prefill(orc, case, kh, vh, causal, kv_dtype=kv_dtype, k_scale=ks, v_scale=vs)
+    U.assert_close(got, ref, what=f"prefill {case.name} causal={causal} dtype={kv_dtype}")
 
 
 def test_fresh_prompt_first_row_is_its_value(orc):
@@ -193,11 +207,11 @@ def test_graph_replay_is_bit_exact():
 
 def test_unsupported_forms_are_refused():
     from paged_kv_split_gb300 import binding as B
-    case = inputs.make_prefill_case("unsup", [40], [8], 8, 2, 64, 16, seed=67)
+    case = inputs.make_prefill_case("unsup", [40], [8], 8, 2, 512, 16, seed=67)
     kc, vc = U.gpu_write_cache(case, 0)
     q = U.bf16_dev(case.q)
     out = torch.empty_like(q)
-    for kw in ({"kv_dtype": 1}, {"kv_dtype": 2}):
+    for kw in ({"kv_dtype": 0}, {"kv_dtype": 2}):  # head_dim 512 is not built for prefill
         with pytest.raises(B.PdError):
             B.pd_prefill(q, U.to_dev(case.extra["cu_q"]), kc, vc, U.to_dev(case.block_tables),
                          U.to_dev(case.seq_lens), out, max_q_len=8,

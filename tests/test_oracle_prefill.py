@@ -19,6 +19,7 @@ PREFILL_CASES = [
     ([64, 31], [40, 3], 16, 2, 128, 32, 0),
     ([69, 50], [23, 50], 4, 1, 64, 16, 20),
     ([48], [48], 8, 8, 64, 16, 16),
+    ([90, 37], [30, 37], 4, 2, 256, 32, 0),
 ]
 
 
