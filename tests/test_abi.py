@@ -161,7 +161,8 @@ def test_reshape_and_cache_validation(pdlib):
 
 
 def test_prefill_validation(pdlib):
-    """pd_prefill refuses bad shapes on the host; the pointers are never touched."""
+    """pd_prefill refuses bad shapes on the host; the pointers are never touched
+    (every call here must fail a check: a valid one would launch on them)."""
     _, L = pdlib
     f = L.pd_prefill
     P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
@@ -178,8 +179,9 @@ def test_prefill_validation(pdlib):
                  a["causal"], a["W"], a["dt"], a["ks"], a["vs"], None)
     assert call(B=0) == 0                 # nothing to do, no launch
     assert call(mq=0) == 0
-    assert call(dt=1) == 2                # FP8 / NVFP4 caches: not built for prefill
-    assert call(dt=2) == 2
+    assert call(dt=7) == 2                # unknown cache form
+    assert call(dt=1, ks=0.0) == 1        # FP8 cache: scales must be positive and finite
+    assert call(dt=1, vs=float("nan")) == 1
     assert call(D=512) == 2               # head_dim 512: not built for prefill
     assert call(D=96) == 2
     assert call(bs=8) == 2
