@@ -167,16 +167,40 @@ __global__ void __launch_bounds__(kThreads) partial_simple_kernel(const DecodeAr
   }
 }
 
-// Combine: one CTA of D/4 threads per (q head, sequence); each thread owns
-// 4 consecutive output elements. The split weights w_s = l_s 2^(m_s - M)
-// are computed once, split-parallel across lanes, into shared memory; the
-// weighted sum over the splits then issues its loads four splits at a time.
-template <int D, bool E4M3_OUT>
-__global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
+// Combine: one CTA per (q head, sequence). D/4 threads span one row (4
+// consecutive elements each) and WAYS such lane groups share out the
+// partials: group j sums partials j, j + WAYS, ... Each thread's first kRows
+// partial rows are loaded before the split weights are reduced, so the row
+// loads and the (m, l) loads travel together; the groups' sums are then added
+// in group order through shared memory. Weights w_s = l_s 2^(m_s - M). The
+// host picks WAYS from the largest partial count (one group when a row has
+// only a few partials, as in the balanced schedule: small CTAs).
+template <int D, int WAYS>
+struct CombineShape {
+  static constexpr int kLanes = D / 4;          // threads across a row
+  static constexpr int kThreads = kLanes * WAYS;
+  static constexpr int kRows = 8;               // rows in flight per thread
+};
+
+__device__ __forceinline__ void fma4(float4& acc, float w, const float4& o) {
+  acc.x = fmaf(w, o.x, acc.x);
+  acc.y = fmaf(w, o.y, acc.y);
+  acc.z = fmaf(w, o.z, acc.z);
+  acc.w = fmaf(w, o.w, acc.w);
+}
+
+template <int D, int WAYS, bool E4M3_OUT>
+__global__ void __launch_bounds__(CombineShape<D, WAYS>::kThreads)
+    combine_kernel(const CombineArgs a) {
   // Launched as a programmatic dependent of the partial kernel: wait until
   // that grid has completed and its workspace writes are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  constexpr int kThreads = D / 4;
+  using CS = CombineShape<D, WAYS>;
+  constexpr int kThreads = CS::kThreads;
+  constexpr int kWarps = (kThreads + 31) / 32;
+  // lanes of the (possibly partial) warp and the first butterfly offset
+  constexpr unsigned kMask = kThreads >= 32 ? 0xFFFFFFFFu : ((1u << kThreads) - 1u);
+  constexpr int kOff = kThreads >= 32 ? 16 : kThreads / 2;
   const int h = blockIdx.x;
   const int b = blockIdx.y;
   // partial s of this (sequence, q head) is workspace row row0 + s * stride
@@ -203,21 +227,34 @@ __global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
     stride = 1;
   }
   const int tid = threadIdx.x;
-  // lanes of the (possibly partial) warp and the first butterfly offset
-  constexpr unsigned kMask = kThreads >= 32 ? 0xFFFFFFFFu : ((1u << kThreads) - 1u);
-  constexpr int kOff = kThreads >= 32 ? 16 : kThreads / 2;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int j = tid / CS::kLanes;        // partial group (0 .. WAYS-1)
+  const int d = (tid % CS::kLanes) * 4;  // first of this thread's 4 elements
   __shared__ float w[1024];  // S <= 1024
-  __shared__ float red[2][(kThreads + 31) / 32];
+  __shared__ float red[2][kWarps];
+  __shared__ __align__(16) float part[WAYS > 1 ? WAYS - 1 : 1][WAYS > 1 ? D : 4];
+  const float* op = a.ws_o + row0 * D + d;
+  const int64_t ostep = static_cast<int64_t>(stride) * D;  // between consecutive partials
+  // this thread's first kRows partial rows, in flight during the reductions
+  float4 o[CS::kRows];
+#pragma unroll
+  for (int r = 0; r < CS::kRows; ++r) {
+    const int s = j + r * WAYS;
+    o[r] = s < n ? *reinterpret_cast<const float4*>(op + s * ostep)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   // M = max_s m_s
   float M = -INFINITY;
   for (int s = tid; s < n; s += kThreads) M = fmaxf(M, a.ws_ml[row0 + s * stride].x);
 #pragma unroll
-  for (int o = kOff; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kMask, M, o));
-  if constexpr (kThreads > 32) {
-    if ((tid & 31) == 0) red[0][tid >> 5] = M;
+  for (int off = kOff; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kMask, M, off));
+  if constexpr (kWarps > 1) {
+    if (lane == 0) red[0][warp] = M;
     __syncthreads();
     M = red[0][0];
-    for (int k = 1; k < kThreads / 32; ++k) M = fmaxf(M, red[0][k]);
+#pragma unroll
+    for (int k = 1; k < kWarps; ++k) M = fmaxf(M, red[0][k]);
   }
   // w_s and their sum
   float wsum = 0.0f;
@@ -228,39 +265,49 @@ __global__ void __launch_bounds__(D / 4) combine_kernel(const CombineArgs a) {
     wsum += ws;
   }
 #pragma unroll
-  for (int o = kOff; o > 0; o >>= 1) wsum += __shfl_xor_sync(kMask, wsum, o);
-  if constexpr (kThreads > 32) {
-    if ((tid & 31) == 0) red[1][tid >> 5] = wsum;
+  for (int off = kOff; off > 0; off >>= 1) wsum += __shfl_xor_sync(kMask, wsum, off);
+  if constexpr (kWarps > 1) {
+    if (lane == 0) red[1][warp] = wsum;
   }
-  __syncthreads();
-  if constexpr (kThreads > 32) {
+  __syncthreads();  // also publishes w[]
+  if constexpr (kWarps > 1) {
     wsum = red[1][0];
-    for (int k = 1; k < kThreads / 32; ++k) wsum += red[1][k];
+#pragma unroll
+    for (int k = 1; k < kWarps; ++k) wsum += red[1][k];
   }
-  // out = sum_s w_s O_s / sum_s w_s
-  const int d = tid * 4;
-  const float* op = a.ws_o + row0 * D + d;
-  const int64_t ostep = static_cast<int64_t>(stride) * D;  // between consecutive partials
+  // this group's share of sum_s w_s O_s
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  int s = 0;
-  for (; s + 4 <= n; s += 4) {
-    const float4 o0 = *reinterpret_cast<const float4*>(op + s * ostep);
-    const float4 o1 = *reinterpret_cast<const float4*>(op + (s + 1) * ostep);
-    const float4 o2 = *reinterpret_cast<const float4*>(op + (s + 2) * ostep);
-    const float4 o3 = *reinterpret_cast<const float4*>(op + (s + 3) * ostep);
-    const float w0 = w[s], w1 = w[s + 1], w2 = w[s + 2], w3 = w[s + 3];
-    acc.x = fmaf(w0, o0.x, fmaf(w1, o1.x, fmaf(w2, o2.x, fmaf(w3, o3.x, acc.x))));
-    acc.y = fmaf(w0, o0.y, fmaf(w1, o1.y, fmaf(w2, o2.y, fmaf(w3, o3.y, acc.y))));
-    acc.z = fmaf(w0, o0.z, fmaf(w1, o1.z, fmaf(w2, o2.z, fmaf(w3, o3.z, acc.z))));
-    acc.w = fmaf(w0, o0.w, fmaf(w1, o1.w, fmaf(w2, o2.w, fmaf(w3, o3.w, acc.w))));
+#pragma unroll
+  for (int r = 0; r < CS::kRows; ++r) {
+    const int s = j + r * WAYS;
+    if (s < n) fma4(acc, w[s], o[r]);
   }
-  for (; s < n; ++s) {
-    const float4 o = *reinterpret_cast<const float4*>(op + s * ostep);
-    const float ws = w[s];
-    acc.x = fmaf(ws, o.x, acc.x);
-    acc.y = fmaf(ws, o.y, acc.y);
-    acc.z = fmaf(ws, o.z, acc.z);
-    acc.w = fmaf(ws, o.w, acc.w);
+  for (int s0 = j + CS::kRows * WAYS; s0 < n; s0 += CS::kRows * WAYS) {
+#pragma unroll
+    for (int r = 0; r < CS::kRows; ++r) {
+      const int s = s0 + r * WAYS;
+      o[r] = s < n ? *reinterpret_cast<const float4*>(op + s * ostep)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int r = 0; r < CS::kRows; ++r) {
+      const int s = s0 + r * WAYS;
+      if (s < n) fma4(acc, w[s], o[r]);
+    }
+  }
+  // groups 1.. hand their sums to group 0, which adds them in group order
+  if constexpr (WAYS > 1) {
+    if (j > 0) *reinterpret_cast<float4*>(&part[j - 1][d]) = acc;  // NOLINT
+    __syncthreads();
+    if (j > 0) return;
+#pragma unroll
+    for (int k = 0; k < WAYS - 1; ++k) {
+      const float4 p = *reinterpret_cast<const float4*>(&part[k][d]);
+      acc.x += p.x;
+      acc.y += p.y;
+      acc.z += p.z;
+      acc.w += p.w;
+    }
   }
   const float inv = 1.0f / fmaxf(wsum, 1e-20f);
   if constexpr (E4M3_OUT) {
@@ -334,13 +381,13 @@ cudaError_t launch_decode_partial(const DecodeArgs& a, int head_dim, int kv_dtyp
   }
 }
 
-template <int D>
+template <int D, int WAYS>
 cudaError_t launch_combine_pdl(const CombineArgs& a, cudaStream_t st) {
   // Programmatic dependent launch: the combine grid may be scheduled while the
   // partial kernel drains; griddepcontrol.wait inside keeps it correct.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.num_q_heads, a.num_seqs);
-  cfg.blockDim = dim3(D / 4);
+  cfg.blockDim = dim3(CombineShape<D, WAYS>::kThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -348,18 +395,38 @@ cudaError_t launch_combine_pdl(const CombineArgs& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (a.out8 != nullptr) return cudaLaunchKernelEx(&cfg, combine_kernel<D, true>, a);
-  return cudaLaunchKernelEx(&cfg, combine_kernel<D, false>, a);
+  if (a.out8 != nullptr) return cudaLaunchKernelEx(&cfg, combine_kernel<D, WAYS, true>, a);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<D, WAYS, false>, a);
 }
 
-cudaError_t launch_decode_combine(const CombineArgs& a, int head_dim, cudaStream_t st) {
+// Lane groups for rows of up to max_parts partials: enough that each
+// thread's first kRows loads cover them (a power of two), at most 256
+// threads a CTA.
+template <int D>
+cudaError_t launch_combine_ways(const CombineArgs& a, int max_parts, cudaStream_t st) {
+  constexpr int kRows = CombineShape<D, 1>::kRows;
+  constexpr int kMaxWays = (1024 / D) < 8 ? (1024 / D) : 8;
+  int ways = 1;
+  while (ways < kMaxWays && ways * kRows < max_parts) ways *= 2;
+  if constexpr (kMaxWays >= 8) {
+    if (ways == 8) return launch_combine_pdl<D, 8>(a, st);
+  }
+  if constexpr (kMaxWays >= 4) {
+    if (ways == 4) return launch_combine_pdl<D, 4>(a, st);
+  }
+  if (ways == 2) return launch_combine_pdl<D, 2>(a, st);
+  return launch_combine_pdl<D, 1>(a, st);
+}
+
+cudaError_t launch_decode_combine(const CombineArgs& a, int head_dim, int max_parts,
+                                  cudaStream_t st) {
   if (a.num_seqs == 0) return cudaSuccess;
   cudaError_t e;
   switch (head_dim) {
-    case 64: e = launch_combine_pdl<64>(a, st); break;
-    case 128: e = launch_combine_pdl<128>(a, st); break;
-    case 256: e = launch_combine_pdl<256>(a, st); break;
-    case 512: e = launch_combine_pdl<512>(a, st); break;
+    case 64: e = launch_combine_ways<64>(a, max_parts, st); break;
+    case 128: e = launch_combine_ways<128>(a, max_parts, st); break;
+    case 256: e = launch_combine_ways<256>(a, max_parts, st); break;
+    case 512: e = launch_combine_ways<512>(a, max_parts, st); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;

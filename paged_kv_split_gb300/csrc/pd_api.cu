@@ -606,7 +606,8 @@ int pd_decode_combine(const void* workspace, size_t workspace_bytes, const int32
   const CombineArgs c = make_combine_args(num_seqs, num_q_heads, head_dim, block_size,
                                           max_blocks_per_seq, num_splits, sliding_window,
                                           workspace, seq_lens, out);
-  return cuda_status(launch_decode_combine(c, head_dim, static_cast<cudaStream_t>(stream)));
+  return cuda_status(
+      launch_decode_combine(c, head_dim, num_splits, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"
@@ -651,12 +652,12 @@ int decode_split(const void* q, const void* k_cache, const void* v_cache,
     const cudaError_t e = cuda_core ? launch_decode_partial(a, head_dim, kv_dtype, st)
                                     : launch_decode_partial_mma(a, head_dim, kv_dtype, st);
     if (e != cudaSuccess) return PD_ERR_CUDA;
-    return cuda_status(launch_decode_combine(c, head_dim, st));
+    return cuda_status(launch_decode_combine(c, head_dim, S, st));
   }
   if (cuda_core) {
     // the CUDA-core cross-check kernel writes every partial; the combine merges all
     if (launch_decode_partial(a, head_dim, kv_dtype, st) != cudaSuccess) return PD_ERR_CUDA;
-    return cuda_status(launch_decode_combine(c, head_dim, st));
+    return cuda_status(launch_decode_combine(c, head_dim, S, st));
   }
   // the partial kernel writes the rows of sequences whose keys fit one split
   // (and zero rows for empty ones); the combine merges the rest
@@ -664,7 +665,7 @@ int decode_split(const void* q, const void* k_cache, const void* v_cache,
   a.direct = 1;
   if (launch_decode_partial_mma(a, head_dim, kv_dtype, st) != cudaSuccess) return PD_ERR_CUDA;
   c.skip_direct = 1;
-  return cuda_status(launch_decode_combine(c, head_dim, st));
+  return cuda_status(launch_decode_combine(c, head_dim, S, st));
 }
 }  // namespace
 
@@ -801,7 +802,10 @@ int decode_balanced(const void* q, const void* k_cache, const void* v_cache,
   c.plan_seg = pl + lay.seg_off;
   c.num_kv_heads = num_kv_heads;
   if (out_stride) c.out_stride = out_stride;
-  return cuda_status(launch_decode_combine(c, head_dim, st));
+  // a (sequence, kv head) range has ceil(pieces / ranges) pieces on average;
+  // the plan's longest may have more (its rows then take a few more loads)
+  const int64_t avg = segs > 0 ? (num_pieces + segs - 1) / segs : 1;
+  return cuda_status(launch_decode_combine(c, head_dim, static_cast<int>(avg), st));
 }
 }  // namespace
 

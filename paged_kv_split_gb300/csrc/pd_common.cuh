@@ -256,7 +256,9 @@ cudaError_t launch_decode_partial_balanced(const DecodeArgs& a, int head_dim, in
                                            cudaStream_t st);
 // Resident CTAs per SM of the balanced partial kernel for a GQA group size.
 int balanced_ctas_per_sm(int kv_dtype, int head_dim, int group);
-cudaError_t launch_decode_combine(const CombineArgs& a, int head_dim, cudaStream_t st);
+// max_parts: the most partials any row has (sizes the combine's CTAs)
+cudaError_t launch_decode_combine(const CombineArgs& a, int head_dim, int max_parts,
+                                  cudaStream_t st);
 // Paged prefill (head_dim 64 / 128 / 256); grid.x = q tiles.
 // launch_prefill: mma.sync kernel, any cache form, 64 rows per CTA
 // (tokens_per_cta = 64 / G); launch_prefill_umma: tcgen05 kernel, BF16

@@ -149,3 +149,126 @@ def test_partial_then_combine_equals_one_call(orc):
     torch.cuda.synchronize()
     halves = out.view(torch.int16).cpu().numpy().view(np.uint16)
     assert np.array_equal(fused, halves)
+
+
+# ---- workspace contents, skewed plans, graph replays -------------------------
+def _balanced_call(case, kc, vc, plan, pdev, q, out, ws, kv_dtype=0, fn=None):
+    from paged_kv_split_gb300 import binding as B
+    (fn or B.pd_decode_balanced)(q, kc, vc, U.to_dev(case.block_tables), pdev, plan, out,
+                                 num_kv_heads=case.num_kv_heads, block_size=case.block_size,
+                                 num_blocks=case.num_blocks, scale=case.scale,
+                                 sliding_window=case.sliding_window, kv_dtype=kv_dtype,
+                                 workspace=ws)
+
+
+def _bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def test_workspace_contents_do_not_matter(orc):
+    """Whatever the workspace held before the call (zeros, all-ones, random
+    bytes, the previous call's partials for another q) the output has the
+    same bits, equal to the oracle's."""
+    from paged_kv_split_gb300 import binding as B
+    case = inputs.make_case("ws_any", [1500, 40, 0, 2600, 333, 17], 32, 8, 128, 16, seed=21,
+                            extra_blocks=1)
+    case.block_tables[case.block_tables < 0] = 0
+    kc, vc = U.gpu_write_cache(case, 0)
+    ref, _ = U.oracle_decode(orc, case, kc.cpu().numpy(), vc.cpu().numpy(), 0)
+    plan = B.pd_balanced_plan(case.seq_lens, num_q_heads=case.num_q_heads,
+                              num_kv_heads=case.num_kv_heads, head_dim=case.head_dim,
+                              block_size=case.block_size,
+                              max_blocks_per_seq=case.max_blocks_per_seq, num_sms=_sms())
+    assert plan.num_pieces > case.num_seqs * case.num_kv_heads  # some ranges have pieces to merge
+    pdev = plan.to("cuda")
+    q = U.bf16_dev(case.q)
+    nbytes = max(plan.workspace_bytes, 16)
+    fills = [torch.zeros(nbytes, dtype=torch.uint8, device="cuda"),
+             torch.full((nbytes,), 255, dtype=torch.uint8, device="cuda"),
+             torch.from_numpy(inputs.uniform_int(22, nbytes, 0, 255).astype(np.uint8)).cuda()]
+    outs = []
+    for ws in fills:
+        out = torch.full_like(q, float("nan"))
+        _balanced_call(case, kc, vc, plan, pdev, q, out, ws)
+        torch.cuda.synchronize()
+        outs.append(_bits(out))
+    U.assert_close(outs[0], ref, what="balanced, zeroed workspace")
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    # leftovers of a call with another q, then this q again on the same bytes
+    ws = fills[2]
+    q2 = U.bf16_dev(inputs.make_case("ws_any2", list(case.seq_lens), 32, 8, 128, 16,
+                                     seed=23).q)
+    out2 = torch.full_like(q, float("nan"))
+    _balanced_call(case, kc, vc, plan, pdev, q2, out2, ws)
+    out = torch.full_like(q, float("nan"))
+    _balanced_call(case, kc, vc, plan, pdev, q, out, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(out), outs[0])
+    assert not np.array_equal(_bits(out2), outs[0])
+
+
+def test_long_range_among_short_ones(orc):
+    """One long sequence among short ones: few pieces per range on average,
+    so the combine's CTAs are sized for a few partials, but the long
+    sequence's ranges have dozens (several rounds of loads per thread). Equal
+    to the oracle, and bit-equal to the two halves called one by one."""
+    from paged_kv_split_gb300 import binding as B
+    lens = [30000] + [int(x) for x in inputs.uniform_int(24, 63, 1, 200)]
+    case = inputs.make_case("long_among_short", lens, 32, 8, 128, 16, seed=25)
+    kc, vc = U.gpu_write_cache(case, 0)
+    ref, _ = U.oracle_decode(orc, case, kc.cpu().numpy(), vc.cpu().numpy(), 0)
+    got, plan = gpu_decode_balanced(case, kc, vc, 0)
+    segs = case.num_seqs * case.num_kv_heads
+    assert plan.num_pieces <= 8 * segs and plan.num_pieces - segs > 20
+    U.assert_close(got, ref, what="long range among short ones")
+    q = U.bf16_dev(case.q)
+    out = torch.full_like(q, float("nan"))
+    pdev = plan.to("cuda")
+    ws = torch.empty(max(plan.workspace_bytes, 16), dtype=torch.uint8, device="cuda")
+    _balanced_call(case, kc, vc, plan, pdev, q, out, ws, fn=B.pd_decode_balanced_partial)
+    _balanced_call(case, kc, vc, plan, pdev, q, out, ws, fn=B.pd_decode_balanced_combine)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(out), got)
+
+
+@pytest.mark.parametrize("kv_dtype", [0, 1, 2], ids=["bf16", "fp8", "nvfp4"])
+def test_graph_replays_follow_q(orc, kv_dtype):
+    """pd_decode_balanced captured in a CUDA graph: q changes between replays
+    (copied into the captured buffer); each replay equals an eager call on
+    that q."""
+    from paged_kv_split_gb300 import binding as B
+    case = inputs.make_case("graph_bal", [700, 1900, 64, 1200], 16, 4, 128, 16, seed=26)
+    ks, vs = U.fp8_scales(orc, case) if kv_dtype == 1 else (1.0, 1.0)
+    kc, vc = U.gpu_write_cache(case, kv_dtype, ks, vs)
+    plan = B.pd_balanced_plan(case.seq_lens, num_q_heads=case.num_q_heads,
+                              num_kv_heads=case.num_kv_heads, head_dim=case.head_dim,
+                              block_size=case.block_size,
+                              max_blocks_per_seq=case.max_blocks_per_seq, kv_dtype=kv_dtype,
+                              num_sms=_sms())
+    pdev = plan.to("cuda")
+    bt = U.to_dev(case.block_tables)
+    kw = dict(num_kv_heads=case.num_kv_heads, block_size=case.block_size,
+              num_blocks=case.num_blocks, scale=case.scale, kv_dtype=kv_dtype, k_scale=ks,
+              v_scale=vs)
+    qs = [U.bf16_dev(inputs.make_case("graph_bal_q", list(case.seq_lens), 16, 4, 128, 16,
+                                      seed=27 + i).q) for i in range(3)]
+    q = qs[0].clone()
+    out = torch.empty_like(q)
+    ws = torch.empty(max(plan.workspace_bytes, 16), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        B.pd_decode_balanced(q, kc, vc, bt, pdev, plan, out, workspace=ws, stream=s, **kw)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        B.pd_decode_balanced(q, kc, vc, bt, pdev, plan, out, workspace=ws, stream=s, **kw)
+    for qi in qs + qs[::-1]:
+        q.copy_(qi)
+        g.replay()
+        torch.cuda.synchronize()
+        got = _bits(out)
+        eager = torch.full_like(q, float("nan"))
+        B.pd_decode_balanced(qi, kc, vc, bt, pdev, plan, eager, **kw)
+        torch.cuda.synchronize()
+        assert np.array_equal(got, _bits(eager))
