@@ -420,7 +420,8 @@ int pd_decode_static_ws(const void* q, const void* k_cache, const void* v_cache,
  * head_dim 64, 128 or 256, block_size 16 or 32, G = num_q_heads /
  * num_kv_heads <= 16; anything else returns PD_ERR_UNSUPPORTED. No
  * workspace: each query tile writes its rows. BF16 caches run on the tcgen05
- * tensor cores (accumulators in TMEM); FP8 and NVFP4 caches on mma.sync
+ * tensor cores (accumulators in TMEM; at head_dim 64 and 128 two 128-row
+ * query tiles share each CTA's K/V stages); FP8 and NVFP4 caches on mma.sync
  * tiles, each stage widened once to f16 (exact) before its MMAs.
  * Device pointers owned by the caller, 16-byte aligned; enqueued on `stream`,
  * never synchronises. */

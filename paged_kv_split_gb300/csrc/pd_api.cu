@@ -935,6 +935,8 @@ int prefill_impl(const void* q, int64_t q_stride, const int32_t* cu_q, const voi
     return cuda_status(launch_prefill(a, k_cache, v_cache, head_dim, kv_dtype, max_q_len, st));
   }
   a.tokens_per_cta = 128 / G;
+  if (head_dim <= 128)
+    return cuda_status(launch_prefill_pair(a, k_cache, v_cache, head_dim, max_q_len, st));
   return cuda_status(launch_prefill_umma(a, k_cache, v_cache, head_dim, max_q_len, st));
 }
 

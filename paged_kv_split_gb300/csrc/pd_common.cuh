@@ -259,12 +259,16 @@ int balanced_ctas_per_sm(int kv_dtype, int head_dim, int group);
 // max_parts: the most partials any row has (sizes the combine's CTAs)
 cudaError_t launch_decode_combine(const CombineArgs& a, int head_dim, int max_parts,
                                   cudaStream_t st);
-// Paged prefill (head_dim 64 / 128 / 256); grid.x = q tiles.
+// Paged prefill (head_dim 64 / 128 / 256).
 // launch_prefill: mma.sync kernel, any cache form, 64 rows per CTA
-// (tokens_per_cta = 64 / G); launch_prefill_umma: tcgen05 kernel, BF16
-// caches, 128 rows per CTA (128 / G).
+// (tokens_per_cta = 64 / G); launch_prefill_pair: tcgen05 kernel, BF16
+// caches, head_dim 64 / 128, two 128-row query tiles per CTA
+// (tokens_per_cta = 128 / G per tile); launch_prefill_umma: tcgen05 kernel,
+// BF16 caches, head_dim 256, one 128-row tile per CTA (128 / G).
 cudaError_t launch_prefill(const PrefillArgs& a, const void* k_cache, const void* v_cache,
                            int head_dim, int kv_dtype, int max_q_len, cudaStream_t st);
+cudaError_t launch_prefill_pair(const PrefillArgs& a, const void* k_cache, const void* v_cache,
+                                int head_dim, int max_q_len, cudaStream_t st);
 cudaError_t launch_prefill_umma(const PrefillArgs& a, const void* k_cache, const void* v_cache,
                                 int head_dim, int max_q_len, cudaStream_t st);
 }  // namespace pd

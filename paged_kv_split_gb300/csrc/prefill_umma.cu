@@ -1,8 +1,10 @@
 // Paged prefill on the 5th-generation tensor cores (tcgen05, accumulators in
-// TMEM) over the BF16 paged cache. Same semantics and interface as the
-// mma.sync kernel in prefill_mma.cu (which stays as a cross-check): pegainfer
-// issue 1008 (`prefill_paged_launch`), AstrAI "csrc/tests" log (causal offset,
-// stride addressing). Design, for sm_103a:
+// TMEM) over the BF16 paged cache, head_dim 256 (one 128-row query tile per
+// CTA: O takes 256 TMEM columns, so two tiles do not fit; head_dim 64 and 128
+// run two tiles per CTA in prefill_pair.cu). Same semantics and interface as
+// the mma.sync kernel in prefill_mma.cu (which stays as a cross-check):
+// pegainfer issue 1008 (`prefill_paged_launch`), AstrAI "csrc/tests" log
+// (causal offset, stride addressing). Design, for sm_103a:
 //
 //  * One CTA per (query tile, kv head, sequence) owns 128 (token, q head)
 //    rows: 128 / G query tokens times the GQA group's G heads, so every K/V
@@ -40,11 +42,13 @@
 
 #include "mma_common.cuh"
 #include "pd_common.cuh"
+#include "umma_common.cuh"
 
 namespace pd {
 namespace {
 
 using namespace ::pd::mma;
+using namespace ::pd::umma;
 
 // K/V stages of the ring: the copies of a tile must be issued several tiles
 // ahead of its MMAs to cover the loaded memory latency
@@ -107,72 +111,6 @@ struct UCfg {
   static_assert(kCacheStageBytes % 1024 == 0 && kQBytes % 1024 == 0, "1024-byte aligned tiles");
   static_assert(kSmemBytes <= 227 * 1024, "one CTA's shared memory");
 };
-
-// tcgen05 shared-memory matrix descriptor: start address, leading and stride
-// byte offsets (16-byte units), the fixed bit 46, 128-byte swizzle (mode 2).
-__device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) |
-         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
-         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-// Instruction descriptor of kind::f16: f32 accumulator, bf16 A and B, A
-// K-major, B K-major (0) or MN-major (1), N >> 3, M >> 4.
-__host__ __device__ constexpr uint32_t umma_idesc(int M, int N, int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn_major) << 16) |
-         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
-}
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::
-                   "r"(bar)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-        "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                       uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
 
 template <int D, int BS>
 __global__ void __launch_bounds__(kUmmaThreads, PD_UMMA_PREFILL_MIN_BLOCKS)
@@ -635,13 +573,7 @@ cudaError_t launch_prefill_umma(const PrefillArgs& a, const void* k_cache, const
                                 int head_dim, int max_q_len, cudaStream_t st) {
   if (a.num_seqs == 0 || max_q_len == 0) return cudaSuccess;
   const bool bs16 = a.block_size == 16;
-  switch (head_dim) {
-    case 64:
-      return bs16 ? launch_umma_cfg<64, 16>(a, k_cache, v_cache, max_q_len, st)
-                  : launch_umma_cfg<64, 32>(a, k_cache, v_cache, max_q_len, st);
-    case 128:
-      return bs16 ? launch_umma_cfg<128, 16>(a, k_cache, v_cache, max_q_len, st)
-                  : launch_umma_cfg<128, 32>(a, k_cache, v_cache, max_q_len, st);
+  switch (head_dim) {  // head_dim 64 and 128 run on the two-tile kernel (prefill_pair.cu)
     case 256:
       return bs16 ? launch_umma_cfg<256, 16>(a, k_cache, v_cache, max_q_len, st)
                   : launch_umma_cfg<256, 32>(a, k_cache, v_cache, max_q_len, st);

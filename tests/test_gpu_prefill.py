@@ -46,6 +46,10 @@ CASES = [
     ("g16", [150, 60], [33, 60], 16, 1, 64, 32, 0),
     ("g8_window_ragged", [500, 211, 64], [130, 211, 1], 32, 4, 128, 16, 100),
     ("empty_and_zero_q", [0, 90, 40], [0, 0, 40], 8, 2, 64, 16, 0),
+    # two query tiles per CTA: tiles whose windows barely overlap, a partial
+    # second tile, head_dim 64 with 32-row pages
+    ("pair_window_g1", [600, 260], [300, 260], 4, 4, 128, 16, 32),
+    ("pair_g4_bs32", [900, 140], [200, 140], 16, 4, 64, 32, 64),
     ("d256", [300, 77], [130, 77], 8, 2, 256, 16, 0),
     ("d256_g8_window_bs32", [400, 129], [200, 64], 16, 2, 256, 32, 100),
 ]
