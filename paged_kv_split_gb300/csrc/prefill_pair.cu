@@ -357,23 +357,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       }
       tc_fence_after();
       const uint32_t bad = bad_copies[st];
-      float s[64];  // keys t0 + k
-      {
-        uint32_t v[4][16];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld16(s_tm + sb * 64 + c * 16, v[c]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int k = 0; k < 16; ++k) s[c * 16 + k] = __uint_as_float(v[c][k]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(s_free(X, sb)));
-
-      // ---- mask and scale: bit k of `valid` = key t0 + k is in [rlo, rpos]
-      // and its page in the pool ----
+      // ---- bit k of `valid`: key t0 + k is in [rlo, rpos] and its page in
+      // the pool ----
       const int klo_r = max(rlo - t0, 0), khi_r = min(rpos + 1 - t0, 64);  // [klo_r, khi_r)
       uint64_t valid = 0ull;
       if (khi_r > klo_r)
@@ -384,35 +369,95 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           if ((bad >> c) & 1u)
             valid &= ~((C::kBR >= 64 ? ~0ull : ((1ull << C::kBR) - 1ull)) << (c * C::kBR));
       }
-      float mxp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (valid == ~0ull) {
-#pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          s[k] *= sl2;
-          mxp[k & 3] = fmaxf(mxp[k & 3], s[k]);
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          s[k] = ((valid >> k) & 1ull) ? s[k] * sl2 : -INFINITY;
-          mxp[k & 3] = fmaxf(mxp[k & 3], s[k]);
-        }
-      }
-      const float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
-      // the reference max moves only past the threshold (or from -inf)
-      const float mn = (mx > m_run + kRescaleLog2P) ? mx : m_run;
-      const float alpha = (mn == m_run) ? 1.0f : ex2(m_run - mn);
+      // A full tile of a row that has seen keys takes P = 2^(s scale log2e -
+      // m_run) against the current reference right away, the first 32 scores
+      // while the last 32 are still on their way from TMEM. Only if the tile
+      // passes the reference by more than the threshold does the warp read
+      // the scores again and take P against the new reference (the same
+      // rule as taking the tile max first). Other tiles (the row's first,
+      // masked ones) take the max first.
+      const bool fast = valid == ~0ull && m_run != -INFINITY;
+      const uint32_t sbase = s_tm + sb * 64;
+      float p[64];
       float lsp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      if (mn == -INFINITY) {  // nothing seen yet by this row: P = 0
+      float mn = m_run, alpha = 1.0f;
+      {
+        uint32_t v[4][16];
+        tmem_ld16(sbase, v[0]);
+        tmem_ld16(sbase + 16, v[1]);
+        tmem_wait_ld();
+        tmem_ld16(sbase + 32, v[2]);
+        tmem_ld16(sbase + 48, v[3]);
+        float mxp[2] = {-INFINITY, -INFINITY};
+        const float nref = -m_run;
+        if (fast) {
 #pragma unroll
-        for (int k = 0; k < 64; ++k) s[k] = 0.0f;
-      } else {
+          for (int k = 0; k < 32; ++k) {
+            const float x = fmaf(__uint_as_float(v[k >> 4][k & 15]), sl2, nref);
+            mxp[k & 1] = fmaxf(mxp[k & 1], x);
+            p[k] = ex2(x);
+            lsp[k & 3] += p[k];
+          }
+        }
+        tmem_wait_ld();
+        if (fast) {
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          s[k] = ex2(s[k] - mn);
-          lsp[k & 3] += s[k];
+          for (int k = 32; k < 64; ++k) {
+            const float x = fmaf(__uint_as_float(v[k >> 4][k & 15]), sl2, nref);
+            mxp[k & 1] = fmaxf(mxp[k & 1], x);
+            p[k] = ex2(x);
+            lsp[k & 3] += p[k];
+          }
+          const float mx = fmaxf(mxp[0], mxp[1]);  // tile max above the reference
+          if (mx > kRescaleLog2P) {
+            mn = m_run + mx;
+            alpha = ex2(-mx);
+          }
+        } else {
+          float mxq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int k = 0; k < 64; ++k) {
+            const float x = ((valid >> k) & 1ull) ? __uint_as_float(v[k >> 4][k & 15]) * sl2
+                                                  : -INFINITY;
+            p[k] = x;
+            mxq[k & 3] = fmaxf(mxq[k & 3], x);
+          }
+          const float mx = fmaxf(fmaxf(mxq[0], mxq[1]), fmaxf(mxq[2], mxq[3]));
+          // the reference max moves only past the threshold (or from -inf)
+          mn = (mx > m_run + kRescaleLog2P) ? mx : m_run;
+          alpha = (mn == m_run) ? 1.0f : ex2(m_run - mn);
+          if (mn == -INFINITY) {  // nothing seen yet by this row: P = 0
+#pragma unroll
+            for (int k = 0; k < 64; ++k) p[k] = 0.0f;
+          } else {
+#pragma unroll
+            for (int k = 0; k < 64; ++k) {
+              p[k] = ex2(p[k] - mn);
+              lsp[k & 3] += p[k];
+            }
+          }
+        }
+        // a fast row whose reference moved: the scores again, P against it
+        const bool redo = fast && mn != m_run;
+        if (__any_sync(0xFFFFFFFFu, redo)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld16(sbase + c * 16, v[c]);
+          tmem_wait_ld();
+          if (redo) {
+            const float nr = -mn;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) lsp[q] = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 64; ++k) {
+              p[k] = ex2(fmaf(__uint_as_float(v[k >> 4][k & 15]), sl2, nr));
+              lsp[k & 3] += p[k];
+            }
+          }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(s_free(X, sb)));
       l_run = l_run * alpha + ((lsp[0] + lsp[1]) + (lsp[2] + lsp[3]));
       m_run = mn;
 
@@ -462,9 +507,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       // P row m, keys 0..63: eight swizzled 16-byte pieces
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        sts128(p_s + swz128(m * 128 + q * 16), pack_bf16x2(s[q * 8 + 0], s[q * 8 + 1]),
-               pack_bf16x2(s[q * 8 + 2], s[q * 8 + 3]), pack_bf16x2(s[q * 8 + 4], s[q * 8 + 5]),
-               pack_bf16x2(s[q * 8 + 6], s[q * 8 + 7]));
+        sts128(p_s + swz128(m * 128 + q * 16), pack_bf16x2(p[q * 8 + 0], p[q * 8 + 1]),
+               pack_bf16x2(p[q * 8 + 2], p[q * 8 + 3]), pack_bf16x2(p[q * 8 + 4], p[q * 8 + 5]),
+               pack_bf16x2(p[q * 8 + 6], p[q * 8 + 7]));
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
