@@ -283,6 +283,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = umma_idesc(128, C::kKT, 0);
       constexpr uint32_t idO = umma_idesc(128, D, 1);
+      // Descriptors are built once: a descriptor's start-address field is the
+      // byte address / 16, so an offset inside a tile is a constant added to
+      // its low word (tiles stay below 256 KB of shared memory). One thread
+      // issues every MMA: per instruction an add and the MMA itself.
+      const uint64_t dqA = umma_desc(s0 + C::kQOff, 16, 1024);
+      const uint64_t dqB = umma_desc(s0 + C::kQOff + C::kQBytes, 16, 1024);
+      const uint64_t dpA = umma_desc(s0 + C::kPOff, 16, 1024);
+      const uint64_t dpB = umma_desc(s0 + C::kPOff + C::kPBytes, 16, 1024);
+      const uint64_t dk0 = umma_desc(ring_s, 16, 1024);
+      const uint64_t dv0 = umma_desc(ring_s + C::kCacheStageBytes, 8192, 1024);
       // S_x(j) = Q_x K_j^T into buffer (j - j0(x)) & 1 of tile x
       auto issue_s = [&](int x, int j) -> bool {
         const int jl = j - j0(x);
@@ -291,14 +301,15 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         if (jl >= 2 && !mbar_wait(smem_u32(s_free(x, jl & 1)), ((jl - 2) >> 1) & 1))
           return false;
         tc_fence_after();
-        const uint32_t kst = ring_s + st * C::kStageBytes;
-        const uint32_t q_s = s0 + C::kQOff + x * C::kQBytes;
+        const uint64_t a0 = x ? dqB : dqA;
+        const uint64_t b0 = dk0 + static_cast<uint64_t>((st * C::kStageBytes) >> 4);
+        const uint32_t d = tmem + x * 128 + (jl & 1) * 64;
 #pragma unroll
         for (int ks = 0; ks < C::kKS; ++ks) {
-          const uint32_t off = (ks >> 2) * (C::kKT * 128) + (ks & 3) * 32;
-          const uint32_t qoff = (ks >> 2) * (128 * 128) + (ks & 3) * 32;
-          umma_f16(tmem + x * 128 + (jl & 1) * 64, umma_desc(q_s + qoff, 16, 1024),
-                   umma_desc(kst + off, 16, 1024), idS, ks > 0 ? 1u : 0u);
+          constexpr int kQChunk = 128 * 128, kKChunk = C::kKT * 128;
+          const uint32_t qoff = ((ks >> 2) * kQChunk + (ks & 3) * 32) >> 4;
+          const uint32_t koff = ((ks >> 2) * kKChunk + (ks & 3) * 32) >> 4;
+          umma_f16(d, a0 + qoff, b0 + koff, idS, ks > 0 ? 1u : 0u);
         }
         umma_commit(smem_u32(s_full(x, jl & 1)));
         return true;
@@ -310,17 +321,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         while (ok && nsA < jA1 && nsA <= j + 1) ok = issue_s(0, nsA++);
         while (ok && nsB < jB1 && nsB <= j + 1) ok = issue_s(1, nsB++);
         if (!ok) break;
-        const uint32_t vst = ring_s + (j % C::kStages) * C::kStageBytes + C::kCacheStageBytes;
+        const uint64_t bv = dv0 + static_cast<uint64_t>(((j % C::kStages) * C::kStageBytes) >> 4);
         for (int x = 0; x < 2; ++x) {
           if (j < j0(x) || j >= j1(x)) continue;
           const int jl = j - j0(x);
           if (!(ok = mbar_wait(smem_u32(p_full(x)), jl & 1))) break;
           tc_fence_after();
-          const uint32_t p_s = s0 + C::kPOff + x * C::kPBytes;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_f16(tmem + 256 + x * 128, umma_desc(p_s + kk * 32, 16, 1024),
-                     umma_desc(vst + kk * 2048, 8192, 1024), idO, (jl > 0 || kk > 0) ? 1u : 0u);
+            umma_f16(tmem + 256 + x * 128, (x ? dpB : dpA) + ((kk * 32) >> 4), bv + ((kk * 2048) >> 4),
+                     idO, (jl > 0 || kk > 0) ? 1u : 0u);
           umma_commit(smem_u32(o_done(x)));
         }
         if (!ok) break;
