@@ -50,6 +50,7 @@ constexpr int kPairProdWarp = 8;
 constexpr int kPairMmaWarp = 9;
 constexpr int kPairThreads = 10 * 32;
 constexpr int kPairTmemCols = 512;
+constexpr int kMaxRanked = 256;  // (sequence, pair) items a CTA ranks by cost
 
 template <int D, int BS>
 struct PairCfg {
@@ -86,15 +87,76 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   using C = PairCfg<D, BS>;
   asm volatile("griddepcontrol.launch_dependents;");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int g = blockIdx.y;
-  const int b = blockIdx.z;
-  const int pair = gridDim.x - 1 - blockIdx.x;  // the longest key ranges first
   const int G = a.group;
   const int TPC = a.tokens_per_cta;  // tokens of one query tile: 128 / G
   const int bs = a.block_size;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw;
+  const uint32_t s0 = smem_u32(smem);
+  if (s0 & 1023u) {  // the swizzled tiles need 1024-byte alignment: refuse, do not guess
+    if (tid == 0) atomicOr(a.flags, PD_DEV_BAD_SMEM);
+    return;
+  }
+
+  // ---- which (sequence, pair of query tiles) and kv head this CTA takes ----
+  // CTAs start in launch order (blockIdx.x fastest), one per SM at a time, so
+  // the grid runs as a list schedule: CTA k takes the (k / Hkv)-th costliest
+  // (sequence, pair) item, costs being the pair's key tiles plus two for its
+  // start and end (longest first bounds the tail). Every CTA ranks all items
+  // itself, from cu_q and seq_lens; above kMaxRanked items it takes them in
+  // grid order instead, each sequence's last pair (the most keys) first.
+  int g, b, pair;
+  {
+    const int PM = gridDim.x;  // pair slots per sequence
+    const int n = PM * static_cast<int>(gridDim.z);
+    if (n <= kMaxRanked) {
+      const int k = blockIdx.x + PM * (blockIdx.y + gridDim.y * blockIdx.z);
+      g = k % gridDim.y;
+      const int r = k / gridDim.y;
+      int* cost_s = reinterpret_cast<int*>(smem + C::kPOff);  // P buffers: free until then
+      volatile int* pick_s = cost_s + kMaxRanked;
+      for (int i = tid; i < n; i += kPairThreads) {
+        const int bi = i / PM, t0 = (i % PM) * 2 * TPC;
+        const int ql = a.cu_q[bi + 1] - a.cu_q[bi];
+        const int Li = a.seq_lens[bi];
+        int c = -1;  // no query rows: ranked last
+        if (ql > 0 && t0 < ql) {
+          c = 0;
+          if (Li >= ql && Li <= a.max_blocks_per_seq * bs) {
+            const int pf = a.causal ? Li - ql + t0 : Li - 1;
+            const int pl = a.causal ? Li - ql + min(t0 + 2 * TPC, ql) - 1 : Li - 1;
+            const int lo = (a.sliding_window > 0 && pf + 1 > a.sliding_window)
+                               ? pf + 1 - a.sliding_window
+                               : 0;
+            c = (pl + 1 - (lo / bs) * bs + C::kKT - 1) / C::kKT + 2;
+          }
+        }
+        cost_s[i] = c;
+      }
+      __syncthreads();
+      for (int i = tid; i < n; i += kPairThreads) {
+        const int ci = cost_s[i];
+        int rank = 0;
+        for (int j2 = 0; j2 < n; ++j2) {
+          const int cj = cost_s[j2];
+          rank += (cj > ci || (cj == ci && j2 < i)) ? 1 : 0;
+        }
+        if (rank == r) *pick_s = i;
+      }
+      __syncthreads();
+      const int item = *pick_s;
+      b = item / PM;
+      pair = item % PM;
+    } else {
+      g = blockIdx.y;
+      b = blockIdx.z;
+      pair = PM - 1 - blockIdx.x;
+    }
+  }
 
   // ---- the pair's query tokens and the keys each tile may see ----
   const int q0 = a.cu_q[b];
@@ -135,13 +197,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   auto j0 = [&](int x) { return x ? jB0 : jA0; };
   auto j1 = [&](int x) { return x ? jB1 : jA1; };
 
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = smem_raw;
-  const uint32_t s0 = smem_u32(smem);
-  if (s0 & 1023u) {  // the swizzled tiles need 1024-byte alignment: refuse, do not guess
-    if (tid == 0) atomicOr(a.flags, PD_DEV_BAD_SMEM);
-    return;
-  }
   const uint32_t ring_s = s0 + C::kRingOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* kv_full = bars;
