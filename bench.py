@@ -522,10 +522,11 @@ def measure_workload(args, name, dev, steps=200, warmup=10):
     peak, kind = measured_peaks()
     part = st.partial_ms(min(steps, 100))
     gbs = st.ab["total"] / (ms * 1e-3) / 1e9
-    r = st.roofline(part, peak, kind)
+    r = st.roofline(part, peak, kind, name)
     out = {"us_per_step": round(ms * 1e3, 2), "value": round(gbs, 1), "unit": "GB/s",
            "frac": round(gbs / peak, 4), "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
            "partial_frac": r["frac"], "partial_us": r["partial_us_per_launch"],
+           "partial_traffic": r["traffic"], "partial_algorithmic_bytes": r["algorithmic_bytes_per_launch"],
            "kv_dtype": DTYPE_NAME[case.kv_dtype], "steps": steps, **st.sched,
            "clocks": sampler.summary(w0, w1)}
     del st
