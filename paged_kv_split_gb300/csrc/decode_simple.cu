@@ -170,11 +170,13 @@ __global__ void __launch_bounds__(kThreads) partial_simple_kernel(const DecodeAr
 // Combine: one CTA per (q head, sequence). D/4 threads span one row (4
 // consecutive elements each) and WAYS such lane groups share out the
 // partials: group j sums partials j, j + WAYS, ... Each thread's first kRows
-// partial rows are loaded before the split weights are reduced, so the row
-// loads and the (m, l) loads travel together; the groups' sums are then added
-// in group order through shared memory. Weights w_s = l_s 2^(m_s - M). The
-// host picks WAYS from the largest partial count (one group when a row has
-// only a few partials, as in the balanced schedule: small CTAs).
+// partial rows and their (m, l) are loaded before the weights are found, so
+// they all travel together; every warp finds M = max m_s and the weight sum
+// by itself with shuffles (no block barrier), and the groups' sums are added
+// in group order through shared memory (the one barrier). Weights
+// w_s = l_s 2^(m_s - M). The host picks WAYS from the largest partial count
+// (one group when a row has only a few partials, as in the balanced
+// schedule: small CTAs).
 template <int D, int WAYS>
 struct CombineShape {
   static constexpr int kLanes = D / 4;          // threads across a row
@@ -197,7 +199,6 @@ __global__ void __launch_bounds__(CombineShape<D, WAYS>::kThreads)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   using CS = CombineShape<D, WAYS>;
   constexpr int kThreads = CS::kThreads;
-  constexpr int kWarps = (kThreads + 31) / 32;
   // lanes of the (possibly partial) warp and the first butterfly offset
   constexpr unsigned kMask = kThreads >= 32 ? 0xFFFFFFFFu : ((1u << kThreads) - 1u);
   constexpr int kOff = kThreads >= 32 ? 16 : kThreads / 2;
@@ -228,59 +229,45 @@ __global__ void __launch_bounds__(CombineShape<D, WAYS>::kThreads)
   }
   const int tid = threadIdx.x;
   const int lane = tid & 31;
-  const int warp = tid >> 5;
   const int j = tid / CS::kLanes;        // partial group (0 .. WAYS-1)
   const int d = (tid % CS::kLanes) * 4;  // first of this thread's 4 elements
-  __shared__ float w[1024];  // S <= 1024
-  __shared__ float red[2][kWarps];
   __shared__ __align__(16) float part[WAYS > 1 ? WAYS - 1 : 1][WAYS > 1 ? D : 4];
+  const float2* mlp = a.ws_ml + row0;
   const float* op = a.ws_o + row0 * D + d;
   const int64_t ostep = static_cast<int64_t>(stride) * D;  // between consecutive partials
-  // this thread's first kRows partial rows, in flight during the reductions
+  // this thread's first kRows partial rows and their (m, l), in flight while
+  // the weights are found
   float4 o[CS::kRows];
+  float2 mlr[CS::kRows];
 #pragma unroll
   for (int r = 0; r < CS::kRows; ++r) {
     const int s = j + r * WAYS;
     o[r] = s < n ? *reinterpret_cast<const float4*>(op + s * ostep)
                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    mlr[r] = s < n ? mlp[s * stride] : make_float2(-INFINITY, 0.0f);
   }
-  // M = max_s m_s
+  // every warp finds M = max_s m_s and W = sum_s l_s 2^(m_s - M) by itself
+  // (lanes stride over the partials, shuffles combine): no block barrier
+  constexpr int kWL = kThreads >= 32 ? 32 : kThreads;  // lanes of a warp
   float M = -INFINITY;
-  for (int s = tid; s < n; s += kThreads) M = fmaxf(M, a.ws_ml[row0 + s * stride].x);
+  for (int s = lane; s < n; s += kWL) M = fmaxf(M, mlp[s * stride].x);
 #pragma unroll
   for (int off = kOff; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kMask, M, off));
-  if constexpr (kWarps > 1) {
-    if (lane == 0) red[0][warp] = M;
-    __syncthreads();
-    M = red[0][0];
-#pragma unroll
-    for (int k = 1; k < kWarps; ++k) M = fmaxf(M, red[0][k]);
-  }
-  // w_s and their sum
   float wsum = 0.0f;
-  for (int s = tid; s < n; s += kThreads) {
-    const float2 ml = a.ws_ml[row0 + s * stride];
-    const float ws = (M == -INFINITY) ? 0.0f : ml.y * exp2f(ml.x - M);
-    w[s] = ws;
-    wsum += ws;
-  }
+  if (M != -INFINITY)
+    for (int s = lane; s < n; s += kWL) {
+      const float2 ml = mlp[s * stride];
+      wsum += ml.y * exp2f(ml.x - M);
+    }
 #pragma unroll
   for (int off = kOff; off > 0; off >>= 1) wsum += __shfl_xor_sync(kMask, wsum, off);
-  if constexpr (kWarps > 1) {
-    if (lane == 0) red[1][warp] = wsum;
-  }
-  __syncthreads();  // also publishes w[]
-  if constexpr (kWarps > 1) {
-    wsum = red[1][0];
-#pragma unroll
-    for (int k = 1; k < kWarps; ++k) wsum += red[1][k];
-  }
+  auto weight = [&](const float2 ml) { return (M == -INFINITY) ? 0.0f : ml.y * exp2f(ml.x - M); };
   // this group's share of sum_s w_s O_s
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int r = 0; r < CS::kRows; ++r) {
     const int s = j + r * WAYS;
-    if (s < n) fma4(acc, w[s], o[r]);
+    if (s < n) fma4(acc, weight(mlr[r]), o[r]);
   }
   for (int s0 = j + CS::kRows * WAYS; s0 < n; s0 += CS::kRows * WAYS) {
 #pragma unroll
@@ -288,11 +275,12 @@ __global__ void __launch_bounds__(CombineShape<D, WAYS>::kThreads)
       const int s = s0 + r * WAYS;
       o[r] = s < n ? *reinterpret_cast<const float4*>(op + s * ostep)
                    : make_float4(0.f, 0.f, 0.f, 0.f);
+      mlr[r] = s < n ? mlp[s * stride] : make_float2(-INFINITY, 0.0f);
     }
 #pragma unroll
     for (int r = 0; r < CS::kRows; ++r) {
       const int s = s0 + r * WAYS;
-      if (s < n) fma4(acc, w[s], o[r]);
+      if (s < n) fma4(acc, weight(mlr[r]), o[r]);
     }
   }
   // groups 1.. hand their sums to group 0, which adds them in group order
