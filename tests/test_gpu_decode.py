@@ -223,3 +223,16 @@ def test_sliding_window_d256(orc):
 @pytest.mark.parametrize("kv_dtype", [1, 2], ids=["fp8", "nvfp4"])
 def test_quantised_batch64(orc, kv_dtype):
     run_parity(orc, inputs.quantised(kv_dtype), kv_dtype, [0], check_cache=True)
+
+
+@pytest.mark.parametrize("d,splits", [(64, (130, 400)), (128, (100, 257)), (256, (70, 150))])
+def test_many_splits_per_row(orc, d, splits):
+    """Split counts far above a combine CTA's first round of loads (its lane
+    groups x 8 rows): the combine takes the rest in further rounds, the
+    lane-group count capped by its 256 threads."""
+    case = inputs.make_case(f"many_splits_d{d}", [16000, 2100], 8, 2, d, 16, seed=31 + d)
+    kc, vc = U.gpu_write_cache(case, 0)
+    ref, _ = U.oracle_decode(orc, case, kc.cpu().numpy(), vc.cpu().numpy(), 0)
+    for S in splits:
+        got = U.gpu_decode(case, kc, vc, 0, S)
+        U.assert_close(got, ref, what=f"D={d} S={S}")
