@@ -79,8 +79,9 @@ def test_small_parity(orc, kv_dtype, spec):
 
 
 def test_two_step_partial_then_combine(orc):
-    """pd_decode_partial + pd_decode_combine (two launches) agree with the oracle
-    like pd_decode (one launch, combine fused into the partial kernel)."""
+    """pd_decode_partial + pd_decode_combine (two calls) agree with the oracle
+    like pd_decode (the same two kernels in one call, the combine launched as
+    a programmatic dependent of the partial kernel)."""
     from paged_kv_split_gb300 import binding
     case = inputs.make_case("twostep", [700, 33, 1290, 0], 32, 8, 128, 16, seed=21)
     case.block_tables[case.block_tables < 0] = 0
