@@ -84,7 +84,9 @@ struct Cfg {
   static constexpr int kCacheStageBytes = (kDataBytes + kScaleBytes + 1023) / 1024 * 1024;
   static constexpr int kStageBytes = 2 * kCacheStageBytes;
   static constexpr int kStagesRaw =
-      (kDSplit == 1 ? ring_bytes_small_d<FMT>() : PD_MMA_RING_BYTES_LARGE_D) / kStageBytes;
+      (kDSplit == 1 ? ring_bytes_small_d<FMT>()
+                    : (D == 256 ? PD_MMA_RING_BYTES_SPLIT_D256 : PD_MMA_RING_BYTES_LARGE_D)) /
+      kStageBytes;
   static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
   static constexpr int kRingBytes = kStages * kStageBytes;
   // cross-warp score sums (head_dim split): 2 buffers x 4 warps x m-tiles x 32 lanes x 4*NT
@@ -515,14 +517,17 @@ int mma_ctas_per_sm_estimate(int kv_dtype, int head_dim) {
   auto per_sm = [](int smem) { return (227 * 1024) / (smem + 1024); };
   int smem;
   if (kv_dtype == PD_KV_BF16) {
-    smem = head_dim <= 128 ? Cfg<PD_KV_BF16, 128, 1, 16>::kSmemBytes
-                           : Cfg<PD_KV_BF16, 512, 1, 16>::kSmemBytes;
+    smem = head_dim <= 128   ? Cfg<PD_KV_BF16, 128, 1, 16>::kSmemBytes
+           : head_dim == 256 ? Cfg<PD_KV_BF16, 256, 1, 16>::kSmemBytes
+                             : Cfg<PD_KV_BF16, 512, 1, 16>::kSmemBytes;
   } else if (kv_dtype == PD_KV_FP8_E4M3) {
-    smem = head_dim <= 128 ? Cfg<PD_KV_FP8_E4M3, 128, 1, 16>::kSmemBytes
-                           : Cfg<PD_KV_FP8_E4M3, 512, 1, 16>::kSmemBytes;
+    smem = head_dim <= 128   ? Cfg<PD_KV_FP8_E4M3, 128, 1, 16>::kSmemBytes
+           : head_dim == 256 ? Cfg<PD_KV_FP8_E4M3, 256, 1, 16>::kSmemBytes
+                             : Cfg<PD_KV_FP8_E4M3, 512, 1, 16>::kSmemBytes;
   } else {
-    smem = head_dim <= 128 ? Cfg<PD_KV_NVFP4, 128, 1, 16>::kSmemBytes
-                           : Cfg<PD_KV_NVFP4, 512, 1, 16>::kSmemBytes;
+    smem = head_dim <= 128   ? Cfg<PD_KV_NVFP4, 128, 1, 16>::kSmemBytes
+           : head_dim == 256 ? Cfg<PD_KV_NVFP4, 256, 1, 16>::kSmemBytes
+                             : Cfg<PD_KV_NVFP4, 512, 1, 16>::kSmemBytes;
   }
   const int n = per_sm(smem);
   return n < 1 ? 1 : (n > 4 ? 4 : n);

@@ -19,12 +19,17 @@ namespace mma {
 
 // Shared-memory budget of the stage ring per CTA (bytes; at least 2 stages):
 // 64 KB lets three CTAs share an SM for head_dim <= 128; the head_dim-split
-// kernels (256 / 512) do better with 96 KB and two CTAs.
+// kernels do better with 96 KB and two CTAs at head_dim 512, and the split
+// kernel with 64 KB and three CTAs at 256 (window D=256 workload: 28.3 ->
+// 26.9 us; wide D=512 with 64 KB: 48.0 -> 49.1).
 #ifndef PD_MMA_RING_BYTES_SMALL_D
 #define PD_MMA_RING_BYTES_SMALL_D (64 * 1024)
 #endif
 #ifndef PD_MMA_RING_BYTES_LARGE_D
 #define PD_MMA_RING_BYTES_LARGE_D (96 * 1024)
+#endif
+#ifndef PD_MMA_RING_BYTES_SPLIT_D256
+#define PD_MMA_RING_BYTES_SPLIT_D256 (64 * 1024)
 #endif
 // per cache form at head_dim <= 128. The quantised stages carry a half (FP8)
 // or a quarter (NVFP4) of BF16's bytes and their consumers are bound by the
