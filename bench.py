@@ -884,6 +884,8 @@ def run_prefill(args, rank, world, local):
         "roofline": {"bound": "tensor",
                      "kernel": ("prefill_mma_kernel (mma.sync bf16, pd_prefill_crosscheck)"
                                 if args.prefill_kernel == "mma_sync"
+                                else "prefill_pair_kernel (tcgen05 bf16, two query tiles per "
+                                     "CTA, TMEM accumulators)" if D <= 128
                                 else "prefill_umma_kernel (tcgen05 bf16, TMEM accumulators)"),
                      "achieved": round(achieved, 1), "peak": peak_t, "peak_source": peak_src,
                      "unit": "TFLOP/s", "frac": round(achieved / peak_t, 4), "traffic": None},
