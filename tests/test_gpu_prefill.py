@@ -5,8 +5,9 @@ cache bytes; the chunked-prefill workload at full size compares sampled
 query rows, each computed by the oracle as its own decode over the keys the
 row sees (the oracle pins make that bit-identical to oracle_prefill).
 Edge cases: empty sequences, a fresh prompt (q_len == L), one query per
-sequence, group sizes that do not divide the CTA's rows, a q_len above
-max_q_len, pages outside the pool, strided rows and graph replay. Every test
+sequence, group sizes that do not divide the CTA's rows, more work items
+than the tcgen05 kernel ranks, a q_len above max_q_len, pages outside the
+pool, strided rows and graph replay. Every test
 runs on both kernels (tcgen05 through pd_prefill, mma.sync through
 pd_prefill_crosscheck)."""
 import functools
@@ -114,6 +115,23 @@ def test_small_parity(orc, spec, causal, kv_dtype):
     got = gpu_prefill(case, kc, vc, causal, kv_dtype=kv_dtype, k_scale=ks, v_scale=vs)
     ref = oracle_prefill(orc, case, kh, vh, causal, kv_dtype=kv_dtype, k_scale=ks, v_scale=vs)
     U.assert_close(got, ref, what=f"prefill {case.name} causal={causal} dtype={kv_dtype}")
+
+
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "full"])
+def test_more_items_than_ranked(orc, causal):
+    """More (sequence, pair of query tiles) items than the tcgen05 kernel ranks
+    by cost (256): 40 sequences, two of them with 500-row chunks, so every
+    sequence has 8 pair slots (320 items) and the CTAs take them in grid
+    order instead; most slots have no rows. Every element against the
+    oracle."""
+    lens = [520, 517] + [30 + 7 * i for i in range(38)]
+    qls = [500, 497] + [1 + i % 5 for i in range(38)]
+    case = inputs.make_prefill_case("many_items", lens, qls, 8, 2, 64, 16, seed=811,
+                                    extra_blocks=2)
+    kc, vc = U.gpu_write_cache(case, 0, 1.0, 1.0)
+    got = gpu_prefill(case, kc, vc, causal)
+    ref = oracle_prefill(orc, case, kc.cpu().numpy(), vc.cpu().numpy(), causal)
+    U.assert_close(got, ref, what=f"prefill many items causal={causal}")
 
 
 def test_fresh_prompt_first_row_is_its_value(orc):
